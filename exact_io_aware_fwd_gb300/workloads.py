@@ -1,0 +1,103 @@
+"""Seeded synthetic attention workloads.
+
+This module only draws inputs; it holds none of the attention arithmetic, so that the CUDA
+library's tests and the fp64 oracle can both consume exactly the same tensors.
+
+Recipe (one generator per workload, ``torch.Generator().manual_seed(seed)`` on the CPU):
+  1. Q, K, V, dO are drawn in that order with ``torch.randn(B, H, N, d)`` (float32), multiplied
+     by their standard deviation and rounded to bfloat16 (round-to-nearest-even);
+  2. if the workload has key padding, ``kv_lens = torch.randint(lo, hi + 1, (B,))`` is drawn
+     next from the same generator.
+Layout: contiguous [B, H, N, d] bfloat16, the order the attention signature uses.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    seed: int
+    sigma_qk: float = 1.0
+    sigma_vdo: float = 1.0
+    kv_len_range: tuple | None = None  # inclusive (lo, hi) of per-batch key lengths
+    oracle_slices: int = 0  # (batch, head) slices the oracle checks at full size (0 = all)
+    notes: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(self.d) ** 0.5
+
+    def flops(self) -> tuple[float, float]:
+        """(forward, backward) FLOPs: 4 N^2 d and 10 N^2 d per head, halved when causal."""
+        per_head = float(self.N) * self.N * self.d
+        f = 4.0 * per_head * self.B * self.H
+        b = 10.0 * per_head * self.B * self.H
+        if self.causal:
+            f, b = f / 2, b / 2
+        return f, b
+
+
+# The five synthetic shapes: a one-head smoke test, the GPT-2-medium attention shape the pages
+# time on A100, a causal mid-length case, the long-context causal case the roofline is quoted
+# on, and a ragged key-padded stress case with large logits.
+WORKLOADS = [
+    Workload("smoke-1x1x128x64", 1, 1, 128, 64, False, seed=0),
+    Workload("gpt2-medium-64x16x1024x64", 64, 16, 1024, 64, False, seed=1, oracle_slices=4),
+    Workload("causal-16x16x4096x128", 16, 16, 4096, 128, True, seed=2, oracle_slices=4),
+    Workload("long-causal-1x32x16384x128", 1, 32, 16384, 128, True, seed=3, oracle_slices=2),
+    Workload("ragged-8x12x2000x128", 8, 12, 2000, 128, False, seed=4, sigma_qk=3.0,
+             kv_len_range=(1000, 2000), oracle_slices=8),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS}
+HEADLINE = WORKLOADS[3]
+
+
+def make_inputs(B, H, N, d, seed, sigma_qk=1.0, sigma_vdo=1.0, kv_len_range=None):
+    """Draw (q, k, v, do, kv_lens) on the CPU; kv_lens is None without key padding."""
+    g = torch.Generator().manual_seed(int(seed))
+
+    def draw(sigma):
+        x = torch.randn((B, H, N, d), generator=g, dtype=torch.float32)
+        if sigma != 1.0:
+            x.mul_(sigma)
+        return x.to(torch.bfloat16)
+
+    q = draw(sigma_qk)
+    k = draw(sigma_qk)
+    v = draw(sigma_vdo)
+    do = draw(sigma_vdo)
+    kv_lens = None
+    if kv_len_range is not None:
+        lo, hi = kv_len_range
+        kv_lens = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    return q, k, v, do, kv_lens
+
+
+def workload_inputs(w: Workload):
+    return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, w.sigma_vdo, w.kv_len_range)
+
+
+def sample_slices(w: Workload, count=None, seed_offset=1000):
+    """Seeded choice of (b, h) slices the oracle checks at full size (a separate generator)."""
+    count = w.oracle_slices if count is None else count
+    total = w.B * w.H
+    if count <= 0 or count >= total:
+        return [(bh // w.H, bh % w.H) for bh in range(total)]
+    g = torch.Generator().manual_seed(w.seed + seed_offset)
+    if count == w.B:
+        # one head per batch: every drawn key length is covered
+        heads = torch.randint(0, w.H, (w.B,), generator=g).tolist()
+        return [(b, h) for b, h in enumerate(heads)]
+    picks = torch.randperm(total, generator=g)[:count].tolist()
+    return [(bh // w.H, bh % w.H) for bh in sorted(picks)]
