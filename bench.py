@@ -1,0 +1,406 @@
+"""Benchmark of the exact-attention hot path (forward + backward) on one GB300.
+
+A step is one pass of the whole path over one batch: fa_fwd, then fa_bwd's three stages
+(preprocess, dK/dV with dQ accumulation, dQ convert).  The metric is attention TFLOPS with the
+pages' convention (4 N^2 d forward + 10 N^2 d backward per head, halved when causal).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Default workload: the long-context causal case (B=1, H=32, N=16384, d=128), whose inputs
+(4 x 134 MB) are larger than the 129 MB L2, so no flush is needed between steps.
+With torchrun (N > 1) every rank runs an independent replica (the path does not shard across
+GPUs); the timed region is bracketed by barriers and the max over ranks is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_io_aware_fwd_gb300.workloads import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, 1\u00d7GB300) and % of dense BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SOURCES_FOR_TRAFFIC = ["exact_io_aware_fwd_gb300/csrc/fa_bwd.cu",
+                       "exact_io_aware_fwd_gb300/csrc/fa_fwd.cu",
+                       "exact_io_aware_fwd_gb300/csrc/sm103.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------- distributed
+def dist_setup(n):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def sources_digest():
+    h = hashlib.sha256()
+    for rel in SOURCES_FOR_TRAFFIC:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(f"{kernel}@{workload}")
+    if not e or e.get("sources") != sources_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.rows = []
+        self._stop = threading.Event()
+        self._proc = None
+        self._thread = None
+
+    def start(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self._proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------------------- oracle timing
+def oracle_row_block(q, k, v, do, causal, scale, kv_len, rows):
+    """One bounded sample of the oracle: forward + backward restricted to a block of query rows
+    (O, LSE, D, dQ of those rows and their contributions to dK, dV).  Returns the credited
+    FLOPs with the metric's convention: 14 d per visible (query, key) pair."""
+    import oracle
+
+    st = oracle.row_statistics(q, k, v, do, scale, causal, kv_len, rows)
+    oracle.key_gradients(q, k, v, do, scale, st["LSE"], st["D"], causal, kv_len, rows=rows)
+    n = k.shape[0]
+    lim = n if kv_len is None else int(kv_len)
+    visible = np.minimum(rows + 1, lim) if causal else np.full(len(rows), lim)
+    return 14.0 * q.shape[1] * float(visible.sum())
+
+
+def cpu_sample_inputs(w, q, k, v, do, kv):
+    b, h = 0, 0
+    f = lambda t: t[b, h].float().numpy().astype(np.float64)  # noqa: E731
+    kv_len = int(kv[b]) if kv is not None else None
+    rows_n = min(w.N, 2048)
+    rows = np.arange(w.N - rows_n, w.N)  # the last rows: the most keys under a causal mask
+    return f(q), f(k), f(v), f(do), kv_len, rows
+
+
+def time_oracle_once(w, q, k, v, do, kv):
+    qs, ks, vs, dos, kv_len, rows = cpu_sample_inputs(w, q, k, v, do, kv)
+    t0 = time.perf_counter()
+    flops = oracle_row_block(qs, ks, vs, dos, w.causal, w.scale, kv_len, rows)
+    dt = time.perf_counter() - t0
+    return flops, dt, f"(b,h)=(0,0), query rows {rows[0]}..{rows[-1]} of N={w.N}: O, LSE, dQ and their dK, dV contributions"
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ------------------------------------------------------------------------------- arms
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return
+    q, k, v, do, kv = workload_inputs(w)
+    times, flops = [], 0.0
+    sample = ""
+    for step in range(args.warmup + args.steps):
+        f, dt, sample = time_oracle_once(w, q, k, v, do, kv)
+        if step >= args.warmup:
+            times.append(dt)
+            flops = f
+    total = sum(times)
+    value = flops * len(times) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC,
+        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, world, rank, local):
+    import exact_io_aware_fwd_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, v, do, kv = workload_inputs(w)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    stream = torch.cuda.current_stream()
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    kvd = kv.to(dev) if kv is not None else None
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws = fa.workspace_for(qd)
+    f_fwd, f_bwd = w.flops()
+
+    stages = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
+        if evs is not None:
+            evs[1].record(stream)
+        fa.fa_bwd_preprocess(o, dod, lse, ws)
+        if evs is not None:
+            evs[2].record(stream)
+        fa.fa_bwd_dkdv(qd, kd, vd, dod, dk, dv, ws, causal=w.causal, scale=w.scale, kv_lens=kvd)
+        if evs is not None:
+            evs[3].record(stream)
+        fa.fa_bwd_dq_convert(dq, ws, scale=w.scale)
+        if evs is not None:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    st = fa.fa_get_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after warm-up: {fa.fa_status_string(st)}")
+
+    # ---- device-timed region (inputs resident in HBM)
+    clocks = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier(world)
+    st = fa.fa_get_error()
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status after timed region: {fa.fa_status_string(st)}")
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world)
+    stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for i, s in enumerate(stages)}
+    ms_step = ms_total / args.steps
+    value = (f_fwd + f_bwd) * world / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.pin_memory()  # noqa: E731
+        hq, hk, hv, hdo = (pin(t) for t in (q, k, v, do))
+        hkv = pin(kv) if kv is not None else None
+        ho, hdq, hdk, hdv = (torch.empty_like(hq).pin_memory() for _ in range(4))
+        hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo)) + (
+            hkv.numel() * hkv.element_size() if hkv is not None else 0)
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv, hlse))
+
+        def e2e_step():
+            for h, dvc in ((hq, qd), (hk, kd), (hv, vd), (hdo, dod)):
+                dvc.copy_(h, non_blocking=True)
+            if hkv is not None:
+                kvd.copy_(hkv, non_blocking=True)
+            fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
+            fa.fa_bwd(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale, kv_lens=kvd,
+                      dq=dq, dk=dk, dv=dv, workspace=ws)
+            for dvc, h in ((o, ho), (dq, hdq), (dk, hdk), (dv, hdv), (lse, hlse)):
+                h.copy_(dvc, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier(world)
+        torch.cuda.synchronize()
+        a, bv = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        bv.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(bv), world) / args.steps
+        e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        assert fa.fa_get_error() == fa.FA_OK
+
+    if rank != 0:
+        return
+
+    # ---- roofline of the dominant kernel (largest share of the step)
+    peaks, src = load_peaks()
+    dom = max(("fwd", "bwd_dkdv"), key=lambda s: stage_ms[s])
+    dom_flops = f_fwd if dom == "fwd" else f_bwd
+    achieved = dom_flops / (stage_ms[dom] * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel"}[dom]
+    roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"bf16_tflops (burst) of {src}",
+                "traffic": recorded_traffic(kernel_name, w.name)}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        flops_s, dt, sample = time_oracle_once(w, q, k, v, do, kv)
+        cpu = {"value": flops_s / dt / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
+               "kind": "oracle", "sample": sample, "seconds": dt}
+
+    fwd_tf = f_fwd / (stage_ms["fwd"] * 1e-3) / 1e12
+    bwd_ms = stage_ms["bwd_preprocess"] + stage_ms["bwd_dkdv"] + stage_ms["bwd_dq_convert"]
+    line = {
+        "metric": METRIC,
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+                   "kv_lens": None if kv is None else kv.tolist(),
+                   "l2": "inputs larger than L2 (no flush)" if 4 * q.numel() * 2 > 129e6 else
+                   "inputs smaller than L2 (not flushed)",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
+        "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
+        "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,
+        "stage_ms": stage_ms,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = BY_NAME[args.workload]
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_ours(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+"""Thin ctypes binding of libfa_sm103.so with the C-ABI's names.
+
+Only argument marshalling happens here (torch tensors -> device pointers, the current CUDA
+stream, output/workspace allocation through torch's caching allocator).  Every step of the
+computation runs in the library's CUDA kernels; there is no fallback of any kind: if the
+library is missing or the device is not an sm_100-family GPU the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from .build_lib import LIB_PATH
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+
+EXPORTED = [
+    "fa_fwd",
+    "fa_bwd_workspace_size",
+    "fa_bwd",
+    "fa_bwd_preprocess",
+    "fa_bwd_dkdv",
+    "fa_bwd_dq_convert",
+    "fa_get_error",
+    "fa_status_string",
+]
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} (status {status})")
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of libfa_sm103.so."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(p)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, sz, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_preprocess.argtypes = [vp, vp, vp, i, i, i, i, vp, sz, vp]
+    lib.fa_bwd_preprocess.restype = i
+    lib.fa_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, sz, vp]
+    lib.fa_bwd_dkdv.restype = i
+    lib.fa_bwd_dq_convert.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
+    lib.fa_bwd_dq_convert.restype = i
+    lib.fa_get_error.argtypes = [vp]
+    lib.fa_get_error.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_qkv(*ts):
+    ref = ts[0]
+    if ref.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous CUDA bfloat16 tensors")
+        if t.shape != ref.shape:
+            raise ValueError("shape mismatch")
+    return tuple(ref.shape)
+
+
+def _kv(kv_lens, B, device):
+    if kv_lens is None:
+        return None
+    kv = kv_lens.to(device=device, dtype=torch.int32).contiguous()
+    if kv.numel() != B:
+        raise ValueError("kv_lens must have B entries")
+    return kv
+
+
+def _scale(scale):
+    return -1.0 if scale is None else float(scale)
+
+
+def fa_fwd(q, k, v, causal=False, scale=None, kv_lens=None, out=None, lse=None, stream=None):
+    """O, LSE = exact attention of [B,H,N,d] bf16 q, k, v (see include/fa.h)."""
+    B, H, N, d = _check_qkv(q, k, v)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
+    _check_qkv(q, out)
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                               int(bool(causal)), _scale(scale), _ptr(kv), _stream(stream))
+    _check(st, "fa_fwd")
+    return out, lse
+
+
+def fa_bwd_workspace_size(B, H, N, d) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, N, d))
+
+
+def workspace_for(q):
+    B, H, N, d = q.shape
+    nbytes = fa_bwd_workspace_size(B, H, N, d)
+    if nbytes == 0:
+        raise FAError(FA_ERR_INVALID_ARG, "fa_bwd_workspace_size")
+    # torch's allocator returns 512-byte aligned blocks
+    return torch.empty(nbytes, device=q.device, dtype=torch.uint8)
+
+
+def fa_bwd(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dq=None, dk=None,
+           dv=None, workspace=None, stream=None):
+    """dQ, dK, dV of exact attention given the forward's O and LSE (see include/fa.h)."""
+    B, H, N, d = _check_qkv(q, k, v, o, do)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace_for(q) if workspace is None else workspace
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                               _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), _scale(scale),
+                               _ptr(kv), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
+    B, H, N, d = _check_qkv(o, do)
+    st = load_library().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d,
+                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd_preprocess")
+
+
+def fa_bwd_dkdv(q, k, v, do, dk, dv, workspace, causal=False, scale=None, kv_lens=None,
+                stream=None):
+    B, H, N, d = _check_qkv(q, k, v, do, dk, dv)
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B,
+                                    H, N, d, int(bool(causal)), _scale(scale), _ptr(kv),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd_dkdv")
+
+
+def fa_bwd_dq_convert(dq, workspace, scale=None, stream=None):
+    B, H, N, d = _check_qkv(dq)
+    st = load_library().fa_bwd_dq_convert(_ptr(dq), B, H, N, d, _scale(scale), _ptr(workspace),
+                                          workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd_dq_convert")
+
+
+def fa_get_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device status."""
+    return int(load_library().fa_get_error(_stream(stream)))
+
+
+def default_scale(d: int) -> float:
+    return 1.0 / math.sqrt(d)

@@ -1,0 +1,267 @@
+// C-ABI entry points (declared in include/fa.h): argument validation, TMA tensor-map encoding,
+// kernel launches and the device status word.  Nothing here allocates device memory.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+__device__ int g_fa_status = 0;  // first device-side error since the last fa_get_error()
+
+constexpr int kMaxDevices = 64;
+
+int* status_ptr() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t ns = 0;
+  if (ns == 0) {
+    uint64_t ms = 2000;  // a single pipeline wait is normally a few microseconds
+    if (const char* e = std::getenv("FA_WAIT_TIMEOUT_MS")) {
+      const long v = std::strtol(e, nullptr, 10);
+      if (v > 0) ms = static_cast<uint64_t>(v);
+    }
+    ns = ms * 1000000ull;
+  }
+  return ns;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B*H][N][d] bf16 viewed as a 3-D tensor (d, N, B*H); boxes of 64 x 128 x 1 elements with the
+// 128-byte swizzle.  Rows past N are out of bounds: zero-filled on load, dropped on store.
+bool make_tile_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_sizes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  // 128-row tiles of every (b, h) must be addressable with 32-bit coordinates
+  if (N > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+float resolve_scale(float scale, int d) {
+  return (scale < 0.f) ? 1.0f / std::sqrt(static_cast<float>(d)) : scale;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+fa_status check_device() {
+  int dev = 0, major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return (major == 10) ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+fa_status check_workspace(void* ws, size_t bytes, int BH, int N, int d) {
+  if (ws == nullptr) return FA_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return FA_ERR_INVALID_ARG;
+  if (bytes < fa::workspace_layout(BH, N, d).total) return FA_ERR_WORKSPACE;
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA_OK) return 0;
+  return fa::workspace_layout(B * H, N, d).total;
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int N, int d, int causal, float scale, const int32_t* kv_lens, void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if ((st = check_device()) != FA_OK) return st;
+  int* status = status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (!make_tile_map(&tq, Q, BH, N, d) || !make_tile_map(&tk, K, BH, N, d) ||
+      !make_tile_map(&tv, V, BH, N, d) || !make_tile_map(&to, O, BH, N, d))
+    return FA_ERR_CUDA;
+  fa::FwdArgs a{};
+  a.H = H;
+  a.N = N;
+  a.BH = BH;
+  a.num_qblocks = (N + 255) / 256;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = resolve_scale(scale, d) * kLog2e;
+  a.kv_lens = kv_lens;
+  a.lse = LSE;
+  a.status = status;
+  a.timeout_ns = wait_timeout_ns();
+  if (static_cast<long long>(a.num_qblocks) * BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  cudaError_t e = fa::launch_fwd(d, tq, tk, tv, to, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, int H, int N,
+                            int d, void* workspace, size_t workspace_bytes, void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!O || !dO || !LSE) return FA_ERR_INVALID_ARG;
+  if (!aligned16(O) || !aligned16(dO)) return FA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  if ((st = check_workspace(workspace, workspace_bytes, BH, N, d)) != FA_OK) return st;
+  if ((st = check_device()) != FA_OK) return st;
+  const fa::Workspace w = fa::workspace_layout(BH, N, d);
+  char* ws = static_cast<char*>(workspace);
+  cudaError_t e = fa::launch_bwd_preprocess(
+      d, O, dO, LSE, BH, N, reinterpret_cast<float*>(ws + w.lse2_off),
+      reinterpret_cast<float*>(ws + w.delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                      void* dV, int B, int H, int N, int d, int causal, float scale,
+                      const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !dO || !dK || !dV) return FA_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
+      !aligned16(dV))
+    return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  if ((st = check_workspace(workspace, workspace_bytes, BH, N, d)) != FA_OK) return st;
+  if ((st = check_device()) != FA_OK) return st;
+  int* status = status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  if (!make_tile_map(&tq, Q, BH, N, d) || !make_tile_map(&tk, K, BH, N, d) ||
+      !make_tile_map(&tv, V, BH, N, d) || !make_tile_map(&tdo, dO, BH, N, d) ||
+      !make_tile_map(&tdk, dK, BH, N, d) || !make_tile_map(&tdv, dV, BH, N, d))
+    return FA_ERR_CUDA;
+  const fa::Workspace w = fa::workspace_layout(BH, N, d);
+  char* ws = static_cast<char*>(workspace);
+  fa::BwdArgs a{};
+  a.H = H;
+  a.N = N;
+  a.BH = BH;
+  a.num_qtiles = (N + 127) / 128;
+  a.causal = causal ? 1 : 0;
+  a.scale = resolve_scale(scale, d);
+  a.scale_log2 = a.scale * kLog2e;
+  a.kv_lens = kv_lens;
+  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
+  a.delta = reinterpret_cast<const float*>(ws + w.delta_off);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
+  a.status = status;
+  a.timeout_ns = wait_timeout_ns();
+  if (static_cast<long long>(a.num_qtiles) * BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  cudaError_t e =
+      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdk, tdv, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!dQ || !aligned16(dQ)) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  const int BH = B * H;
+  if ((st = check_workspace(workspace, workspace_bytes, BH, N, d)) != FA_OK) return st;
+  if ((st = check_device()) != FA_OK) return st;
+  const fa::Workspace w = fa::workspace_layout(BH, N, d);
+  cudaError_t e = fa::launch_bwd_dq_convert(
+      d, reinterpret_cast<const float*>(static_cast<char*>(workspace) + w.dq_acc_off), dQ, BH, N,
+      resolve_scale(scale, d), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                 int causal, float scale, const int32_t* kv_lens, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+  st = fa_bwd_preprocess(O, dO, LSE, B, H, N, d, workspace, workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  st = fa_bwd_dkdv(Q, K, V, dO, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
+                   workspace_bytes, stream);
+  if (st != FA_OK) return st;
+  return fa_bwd_dq_convert(dQ, B, H, N, d, scale, workspace, workspace_bytes, stream);
+}
+
+fa_status fa_get_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  int* status = status_ptr();
+  if (status == nullptr) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  switch (v) {
+    case 0: return FA_OK;
+    case 4: return FA_ERR_TIMEOUT;
+    default: return FA_ERR_CUDA;
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,538 @@
+// Backward pass kernels.
+//
+// Method (page "FlashAttention：不减少一次注意力计算，为什么反而更快", section 关键设计三):
+// the forward pass saved only O and the per-row log-sum-exp; the backward pass recomputes each
+// score tile S_ij = Q_i K_j^T and P_ij = exp(S_ij - LSE_i) on chip, and uses
+//   D_i = dO_i . O_i,  dP = dO V^T,  dS = P o (dP - D),
+//   dV_j += P_ij^T dO_i,  dK_j += dS_ij^T Q_i,  dQ_i += dS_ij K_j
+// (with the softmax scale applied to dK and dQ by the chain rule through S = scale * Q K^T).
+//
+// Kernels:
+//  bwd_preprocess  D = rowsum(dO o O) and LSE * log2(e) into the workspace (padded rows get
+//                  D = 0 and +inf, which makes their recomputed P exactly 0), and zeroes the
+//                  float32 dQ accumulator.
+//  bwd_dkdv        one CTA per (b, h, 128-key tile j); dK_j and dV_j accumulate in tensor memory
+//                  over the query tiles i (causal: i >= j only).  Per query tile:
+//                    S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (tcgen05, both operands in smem)
+//                    P^T = exp2(S^T * scale * log2 e - LSE_i * log2 e), written back over S^T
+//                    dS^T = P^T o (dP^T - D_i), written back over dP^T and to smem
+//                    dV += P^T dO_i, dK += dS^T Q_i          (A operand read from tensor memory)
+//                    dQ_i = dS K_j                            (A = dS from smem, MN-major)
+//                  and a warpgroup adds dQ_i into the float32 accumulator with vector
+//                  reductions (red.global.add.v4.f32).  Those atomics make the result
+//                  non-deterministic in the last bits, as the pages note for the default
+//                  backward (page "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section
+//                  "反向传播：用重计算代替存储").
+//  bwd_dq_convert  dQ = bf16(scale * accumulator).
+//
+// dQ accumulator layout ("tile-major"): for (b, h), query tile i, column group g (4 floats)
+// and row r of the tile, element (r, 4g + e) is at float index
+//   (((bh * num_qtiles + i) * (d / 4) + g) * 128 + r) * 4 + e,
+// so that 32 consecutive rows of one column group are 512 contiguous bytes and a warp's
+// vector reduction is fully coalesced.
+#include "fa_internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+Workspace workspace_layout(int BH, int N, int d) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t npad = static_cast<size_t>((N + kTileRows - 1) / kTileRows) * kTileRows;
+  Workspace w;
+  w.dq_acc_off = 0;
+  w.lse2_off = up(static_cast<size_t>(BH) * npad * d * sizeof(float));
+  w.delta_off = w.lse2_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  w.total = w.delta_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  return w;
+}
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      ctl_fail(c, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Preprocess: grid (num_qtiles, BH), 256 threads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
+                                                             const __nv_bfloat16* __restrict__ dO,
+                                                             const float* __restrict__ lse, int N,
+                                                             int nqt, float* __restrict__ lse2,
+                                                             float* __restrict__ delta,
+                                                             float* __restrict__ dq_acc) {
+  constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
+  constexpr int RPW = 32 / G;  // rows per warp per pass
+  const int i = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int npad = nqt * 128;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / G, cl = lane % G;
+  for (int rr = warp * RPW + sub; rr < 128; rr += 8 * RPW) {
+    const int q = i * 128 + rr;
+    float acc = 0.f;
+    if (q < N) {
+      const size_t off = (static_cast<size_t>(bh) * N + q) * D + cl * 8;
+      const uint4 o = __ldg(reinterpret_cast<const uint4*>(O + off));
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
+      const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        acc += bf16_lo(ov[e]) * bf16_lo(gv[e]) + bf16_hi(ov[e]) * bf16_hi(gv[e]);
+    }
+#pragma unroll
+    for (int m = G / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (cl == 0) {
+      const size_t idx = static_cast<size_t>(bh) * npad + q;
+      float l2 = INFINITY;
+      if (q < N) {
+        const float l = __ldg(lse + static_cast<size_t>(bh) * N + q);
+        l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;  // a row with no key: P must be 0
+      }
+      lse2[idx] = l2;
+      delta[idx] = (q < N) ? acc : 0.f;
+    }
+  }
+  float4* t = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D);
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int idx = threadIdx.x; idx < 32 * D; idx += 256) t[idx] = z;
+}
+
+// ------------------------------------------------------------------------------------------
+// dQ convert: grid (num_qtiles, BH), 256 threads; thread = (row r, pair of column groups).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                             __nv_bfloat16* __restrict__ dQ, int N,
+                                                             int nqt, float scale) {
+  const int i = blockIdx.x, bh = blockIdx.y;
+  const int r = threadIdx.x & 127;
+  const int q = i * 128 + r;
+  if (q >= N) return;
+  const float* tile = acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D;
+  for (int cp = threadIdx.x >> 7; cp < D / 8; cp += 2) {
+    const float4 a0 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp) * 128 + r) * 4));
+    const float4 a1 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp + 1) * 128 + r) * 4));
+    uint4 o;
+    o.x = pack_bf16(a0.x * scale, a0.y * scale);
+    o.y = pack_bf16(a0.z * scale, a0.w * scale);
+    o.z = pack_bf16(a1.x * scale, a1.y * scale);
+    o.w = pack_bf16(a1.z * scale, a1.w * scale);
+    *reinterpret_cast<uint4*>(dQ + (static_cast<size_t>(bh) * N + q) * D + cp * 8) = o;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// dK / dV kernel
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t kTile = 128u * D * 2u;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTile;
+  static constexpr uint32_t kQ = kV + kTile;       // 2 stages
+  static constexpr uint32_t kDO = kQ + 2 * kTile;  // 2 stages
+  static constexpr uint32_t kDS = kDO + 2 * kTile; // 128 keys x 128 queries bf16
+  static constexpr uint32_t kLse = kDS + 32768;    // 2 stages x 128 floats
+  static constexpr uint32_t kDelta = kLse + 1024;  // 2 stages x 128 floats
+  static constexpr uint32_t kBar = kDelta + 1024;
+  // kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, p_full, dp_full, ds_full,
+  // dq_full, dq_empty, dkdv_full, mma_done
+  static constexpr int kNumBars = 17;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kBytes = kAbort + 4;
+  // TMEM columns
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                    const __grid_constant__ CUtensorMap tmdK,
+                    const __grid_constant__ CUtensorMap tmdV, const BwdArgs a) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* sm = smem_raw + pad;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = bars + 3;
+  uint64_t* do_full = bars + 5;
+  uint64_t* do_empty = bars + 7;
+  uint64_t* s_full = bars + 9;
+  uint64_t* p_full = bars + 10;
+  uint64_t* dp_full = bars + 11;
+  uint64_t* ds_full = bars + 12;
+  uint64_t* dq_full = bars + 13;
+  uint64_t* dq_empty = bars + 14;
+  uint64_t* dkdv_full = bars + 15;
+  uint64_t* mma_done = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const Ctl ctl{abort_flag, a.status, a.timeout_ns};
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  if (pad + L::kBytes > a.smem_bytes) {
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kErrLayout);
+    return;
+  }
+
+  // ---- work item: key tile j (small j first: with a causal mask they have the most work)
+  const int lin = blockIdx.x;
+  const int bh = lin % a.BH;
+  const int j = lin / a.BH;
+  const int b = bh / a.H;
+  const int N = a.N;
+  const int nqt = a.num_qtiles;
+  const int npad = nqt * 128;
+  int kv_len = N;
+  if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  const int i0 = a.causal ? j : 0;
+  const int nI = (j * 128 < kv_len) ? (nqt - i0) : 0;
+
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    for (int k = 0; k < L::kNumBars; ++k) {
+      // P, dS and the dQ release are signalled by the four warps of a warpgroup
+      const bool per_warp = (&bars[k] == p_full) || (&bars[k] == ds_full) || (&bars[k] == dq_empty);
+      mbar_init(&bars[k], per_warp ? 4 : 1);
+    }
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmdO);
+    tma_prefetch_desc(&tmdK);
+    tma_prefetch_desc(&tmdV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0 && nI > 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sm + L::kK + c * 16384, &tmK, kv_full, c * 64, j * 128, bh);
+        tma_load_3d(sm + L::kV + c * 16384, &tmV, kv_full, c * 64, j * 128, bh);
+      }
+      int nq = 0, ndo = 0;
+      for (int it = 0; it < nI; ++it) {
+        const int i = i0 + it, s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&q_empty[s], ph ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&q_full[s], L::kTile + 1024);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm + L::kQ + s * L::kTile + c * 16384, &tmQ, &q_full[s], c * 64, i * 128, bh);
+        const size_t srow = static_cast<size_t>(bh) * npad + i * 128;
+        bulk_load(sm + L::kLse + s * 512, a.lse2 + srow, 512, &q_full[s]);
+        bulk_load(sm + L::kDelta + s * 512, a.delta + srow, 512, &q_full[s]);
+        nq = it + 1;
+        if (!mbar_wait(&do_empty[s], ph ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&do_full[s], L::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm + L::kDO + s * L::kTile + c * 16384, &tmdO, &do_full[s], c * 64, i * 128,
+                      bh);
+        ndo = it + 1;
+      }
+      if (*abort_flag) {
+        drain_wait(kv_full, 0, ctl);
+        for (int it = max(0, nq - 2); it < nq; ++it) drain_wait(&q_full[it & 1], (it >> 1) & 1, ctl);
+        for (int it = max(0, ndo - 2); it < ndo; ++it)
+          drain_wait(&do_full[it & 1], (it >> 1) & 1, ctl);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0 && nI > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major operands
+      constexpr uint32_t idKV = idesc_bf16(128, D, false, true);    // dV, dK: A in TMEM, B MN-major
+      constexpr uint32_t idQ = idesc_bf16(128, D, true, true);      // dQ: A = dS MN-major, B MN-major
+      const uint32_t kb = sbase + L::kK, vb = sbase + L::kV, dsb = sbase + L::kDS;
+      bool ok = mbar_wait(kv_full, 0, ctl);
+      for (int it = 0; ok && it < nI; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        const uint32_t qb = sbase + L::kQ + s * L::kTile;
+        const uint32_t dob = sbase + L::kDO + s * L::kTile;
+        if (!(ok = mbar_wait(&q_full[s], ph, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_i^T
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + L::kColS, sdesc_sw128(kb + off, 16384, 1024),
+                 sdesc_sw128(qb + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        if (!(ok = mbar_wait(&do_full[s], ph, ctl))) break;
+        if (it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tmem + L::kColDP, sdesc_sw128(vb + off, 16384, 1024),
+                 sdesc_sw128(dob + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(dp_full);
+        if (!(ok = mbar_wait(p_full, it & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i   (128 queries, 16 per MMA)
+          mma_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8, sdesc_sw128(dob + kk * 2048, 16384, 1024),
+                 idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(ds_full, it & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
+          mma_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, sdesc_sw128(qb + kk * 2048, 16384, 1024),
+                 idKV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
+          mma_ss(tmem + L::kColDP, sdesc_sw128(dsb + kk * 2048, 16384, 1024),
+                 sdesc_sw128(kb + kk * 2048, 16384, 1024), idQ, kk > 0 ? 1u : 0u);
+        mma_commit(dq_full);
+        mma_commit(&q_empty[s]);
+        mma_commit(&do_empty[s]);
+      }
+      if (ok) mma_commit(dkdv_full);
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0, ctl);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ================= P and dS: one thread per key row of the tile
+    const uint32_t quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int key = j * 128 + r;
+    const bool row_live = key < kv_len;
+    const uint32_t lanes = (quad * 32u) << 16;
+    const uint32_t tS = tmem + lanes + L::kColS;
+    const uint32_t tDP = tmem + lanes + L::kColDP;
+    const float c2 = a.scale_log2;
+    const uint32_t dsb = sbase + L::kDS;
+    for (int it = 0; it < nI; ++it) {
+      const int i = i0 + it, s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait_warp(&q_full[s], ph, ctl)) break;  // LSE and D of this tile are in smem
+      if (!mbar_wait_warp(s_full, it & 1, ctl)) break;
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512);
+      const float* dl = reinterpret_cast<const float*>(sm + L::kDelta + s * 512);
+      const bool diag = a.causal && (i == j);
+      uint32_t p[64];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32];
+        tmem_ld32(tS + 32 * c, sv);
+        tmem_wait_ld();
+        reg_fence(sv);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = 32 * c + 2 * e;
+          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + q);
+          float x0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, -l2.x));
+          float x1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -l2.y));
+          if (diag) {
+            x0 = (r <= q) ? x0 : 0.f;  // key j*128+r > query i*128+q is masked
+            x1 = (r <= q + 1) ? x1 : 0.f;
+          }
+          if (!row_live) x0 = x1 = 0.f;
+          p[16 * c + e] = pack_bf16(x0, x1);
+        }
+      }
+      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+
+      if (!mbar_wait_warp(dp_full, it & 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t dv[32];
+        tmem_ld32(tDP + 32 * c, dv);
+        tmem_wait_ld();
+        reg_fence(dv);
+        uint32_t ds[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = 32 * c + 2 * e;
+          const float2 dd = *reinterpret_cast<const float2*>(dl + q);
+          const float p0 = bf16_lo(p[16 * c + e]), p1 = bf16_hi(p[16 * c + e]);
+          ds[e] = pack_bf16(p0 * (__uint_as_float(dv[2 * e]) - dd.x),
+                            p1 * (__uint_as_float(dv[2 * e + 1]) - dd.y));
+        }
+        // dS^T packed over the dP^T columns already read (A operand of dK += dS^T Q)
+        tmem_st16(tDP + 16 * c, ds);
+        // and to smem as [key row][query], 128-byte swizzled (A operand of dQ = dS K)
+        const uint32_t panel = dsb + (c >> 1) * 16384;
+        const uint32_t g0 = (c & 1) * 4;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          st_shared_v4(panel + sw128_offset(r, g0 + g), ds[4 * g], ds[4 * g + 1], ds[4 * g + 2],
+                       ds[4 * g + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+  } else if (warp >= 8) {
+    // ================= dQ reduction and the dK / dV epilogue: one thread per row
+    const uint32_t quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lanes = (quad * 32u) << 16;
+    const uint32_t tDP = tmem + lanes + L::kColDP;
+    bool ok = true;
+    for (int it = 0; it < nI; ++it) {
+      const int i = i0 + it;
+      if (!(ok = mbar_wait_warp(dq_full, it & 1, ctl))) break;
+      tc_fence_after();
+      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tDP + 32 * c, v);
+        tmem_wait_ld();
+        reg_fence(v);
+        if (c == D / 32 - 1) {  // tensor memory fully read: release it before the reductions
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dq_empty);
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          red_add_v4(tile + ((8 * c + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
+                     __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                     __uint_as_float(v[4 * g + 3]));
+      }
+    }
+    if (ok && nI > 0) ok = mbar_wait_warp(dkdv_full, 0, ctl);
+    if (ok) {
+      if (nI > 0) tc_fence_after();
+      // dV -> V tile buffer, scale * dK -> K tile buffer (bf16, swizzled), then TMA stores
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
+        const float mul = which == 0 ? 1.f : a.scale;
+        const uint32_t buf = sbase + (which == 0 ? L::kV : L::kK);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          if (nI > 0) {
+            tmem_ld32(tmem + lanes + col + 32 * c, v);
+            tmem_wait_ld();
+            reg_fence(v);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          const uint32_t panel = buf + ((32 * c) / 64) * 16384;
+          const uint32_t g0 = ((32 * c) % 64) / 8;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            st_shared_v4(panel + sw128_offset(r, g0 + g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
+                         pk[4 * g + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (quad == 0 && lane == 0 && !*abort_flag) {
+      for (int c = 0; c < D / 64; ++c) {
+        tma_store_3d(&tmdV, sm + L::kV + c * 16384, c * 64, j * 128, bh);
+        tma_store_3d(&tmdK, sm + L::kK + c * 16384, c * 64, j * 128, bh);
+      }
+      bulk_commit();
+      bulk_wait_read0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse, int BH,
+                                  int N, float* lse2, float* delta, float* dq_acc, cudaStream_t s) {
+  const int nqt = (N + 127) / 128;
+  const dim3 grid(nqt, BH);
+  auto o = static_cast<const __nv_bfloat16*>(O);
+  auto g = static_cast<const __nv_bfloat16*>(dO);
+  if (d == 64)
+    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, lse2, delta, dq_acc);
+  else
+    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, lse2, delta, dq_acc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N, float scale,
+                                  cudaStream_t s) {
+  const int nqt = (N + 127) / 128;
+  const dim3 grid(nqt, BH);
+  auto out = static_cast<__nv_bfloat16*>(dQ);
+  if (d == 64)
+    bwd_dq_convert_kernel<64><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale);
+  else
+    bwd_dq_convert_kernel<128><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale);
+  return cudaGetLastError();
+}
+
+namespace {
+template <int D>
+cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
+                          BwdArgs a, cudaStream_t st) {
+  using L = BwdLayout<D>;
+  constexpr uint32_t kMaxSmem = 232448;  // 227 KB, the per-block opt-in limit of sm_100-family GPUs
+  const uint32_t smem = (L::kBytes + 1024 <= kMaxSmem) ? L::kBytes + 1024 : kMaxSmem;
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  a.smem_bytes = smem;
+  const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
+  bwd_dkdv_kernel<D><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
+                            const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t s) {
+  if (d == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  return launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,421 @@
+// Forward kernel: exact attention O = softmax(scale * Q K^T) V and LSE, one CTA per
+// (b, h, 256-row query block) holding two 128-row query tiles that alternate on the tensor core.
+//
+// Method (first page "FlashAttention：不减少一次注意力计算，为什么反而更快", sections 关键设计一
+// and 关键设计二; page "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section
+// "FlashAttention-1：分块与在线 softmax", Fig. 4): for each key tile K_j, V_j the CTA computes
+// S_ij = Q_i K_j^T, updates the running row max m and row sum l, and accumulates the
+// unnormalised output O~ += P~ V_j; O = O~ / l and LSE = m + log l are written once at the end.
+// S_ij and P_ij live only in tensor memory.
+//
+// GB300 design (the pages' A100 tile rules are prior art, not the blueprint):
+//  * warp 0: TMA producer.  Q tiles once, then K_j and V_j through a ring of smem stages with
+//    full/empty mbarriers (page two, section "FlashAttention-3", Fig. 7: producer warps load,
+//    consumer warps compute).
+//  * warp 1: single-thread tcgen05.mma issuer.  S_t = Q_t K_j^T (both operands in smem) and
+//    O_t += P_t V_j with P_t read straight from tensor memory, alternating the two tiles so
+//    that one tile's softmax overlaps the other tile's MMAs (ping-pong of FlashAttention-3).
+//  * warps 4-7 / 8-11: one warpgroup per query tile, one thread per query row: tcgen05.ld of
+//    the S row, row max, exp2 of (S * scale * log2 e - m), P packed to bf16 and stored back
+//    over S in tensor memory, row sum.  O~ is rescaled in tensor memory only when the running
+//    max of some row of the warp moved (conditional rescaling, page two, section
+//    "FlashAttention-4"); results stay exact because l and O~ always use the same reference.
+//  * causal: key tiles past the diagonal are skipped, the diagonal tile is masked element-wise
+//    (page two, FlashAttention-1 section, causal paragraph).
+//  * epilogue: O~ / l -> bf16 -> swizzled smem (over the Q tile) -> TMA store (rows >= N are
+//    clipped by the tensor map); LSE with plain coalesced stores.
+#include "fa_internal.h"
+#include "sm103.cuh"
+
+namespace fa {
+
+namespace {
+
+// Rescale when the running max grows by more than this (log2 units).  Measured on GB300:
+// 8 (a stale reference, FlashAttention-4 style) is 3.5% faster on the long causal case but the
+// row's largest probability is then 2^delta instead of exactly 1 and its bf16 rounding is not
+// cancelled by l; with large logits that pushes O past 1e-2.  0 keeps the exact running max
+// (the O~ correction is still skipped for a warp whose 32 rows all kept their max).
+#ifndef FA_RESCALE_THRESHOLD
+#define FA_RESCALE_THRESHOLD 0.0f
+#endif
+// 1: normalise O~ by the sum of the bf16-rounded P and keep a separate exact sum for LSE
+// (the alternative fix for a stale max; 9% slower, so off by default).
+#ifndef FA_ROUNDED_SUM
+#define FA_ROUNDED_SUM 0
+#endif
+constexpr float kRescaleThreshold = FA_RESCALE_THRESHOLD;
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D>
+struct FwdLayout {
+  static constexpr uint32_t kTile = 128u * D * 2u;  // one 128 x D bf16 tile
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + 2 * kTile;
+  static constexpr uint32_t kV = kK + kStages * kTile;
+  static constexpr uint32_t kBar = kV + kStages * kTile;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_full[2], done
+  static constexpr int kNumBars = 1 + 4 * kStages + 7;
+  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  static constexpr uint32_t kAbort = kTmemSlot + 4;
+  static constexpr uint32_t kBytes = kAbort + 4;
+  // TMEM columns: S_0, S_1 (128 each), O_0, O_1 (D each)
+  static constexpr uint32_t kColS0 = 0, kColO0 = 256;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+// Wait that ignores the abort flag (used only to drain this CTA's own asynchronous work
+// before exit); bounded by the same time limit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      ctl_fail(c, kErrTimeout);
+      return;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+               const FwdArgs a) {
+  using L = FwdLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+  uint8_t* sm = smem_raw + pad;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + S;
+  uint64_t* v_full = k_empty + S;
+  uint64_t* v_empty = v_full + S;
+  uint64_t* s_full = v_empty + S;
+  uint64_t* p_full = s_full + 2;
+  uint64_t* o_full = p_full + 2;
+  uint64_t* mma_done = o_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
+  const Ctl ctl{abort_flag, a.status, a.timeout_ns};
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  if (pad + L::kBytes > a.smem_bytes) {  // cannot happen with the host's sizing; never proceed
+    if (threadIdx.x == 0) atomicCAS(a.status, 0, kErrLayout);
+    return;
+  }
+
+  // ---- work item: heaviest causal blocks first, all heads of a block level together
+  const int lin = blockIdx.x;
+  const int bh = lin % a.BH;
+  const int qb = a.causal ? (a.num_qblocks - 1 - lin / a.BH) : (lin / a.BH);
+  const int b = bh / a.H;
+  const int N = a.N;
+  int kv_len = N;
+  if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  const int q0 = qb * 256;
+  int nb[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt0 = q0 + 128 * t;
+    int nkeys = kv_len;
+    if (a.causal) nkeys = min(nkeys, qt0 + 128);
+    nb[t] = (qt0 < N) ? (nkeys + 127) / 128 : 0;
+  }
+  const int nb_max = max(nb[0], nb[1]);
+
+  // ---- setup
+  if (warp == 0 && lane == 0) {
+    *abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 4);
+      mbar_init(&o_full[t], 1);
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_u32(sm);
+
+  if (warp == 0) {
+    // ================= TMA producer
+    if (lane == 0 && nb_max > 0) {
+      const int ntiles = (nb[1] > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, ntiles * L::kTile);
+      for (int t = 0; t < ntiles; ++t)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64, q0 + 128 * t,
+                      bh);
+      int jk = 0, jv = 0;  // K and V tiles whose copies have been issued
+      for (int j = 0; j < nb_max; ++j) {
+        const int s = j % S;
+        const uint32_t ph = (j / S) & 1;
+        if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&k_full[s], L::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, j * 128,
+                      bh);
+        jk = j + 1;
+        if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
+        mbar_arrive_expect_tx(&v_full[s], L::kTile);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, j * 128,
+                      bh);
+        jv = j + 1;
+      }
+      if (*abort_flag) {
+        // no copy into this CTA's shared memory may still be in flight when the CTA exits
+        drain_wait(q_full, 0, ctl);
+        for (int jj = max(0, jk - S); jj < jk; ++jj) drain_wait(&k_full[jj % S], (jj / S) & 1, ctl);
+        for (int jj = max(0, jv - S); jj < jv; ++jj) drain_wait(&v_full[jj % S], (jj / S) & 1, ctl);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer
+    if (lane == 0 && nb_max > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S = Q K^T, both K-major
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);     // O += P V, V is MN-major
+      bool ok = mbar_wait(q_full, 0, ctl);
+      for (int j = 0; ok && j <= nb_max; ++j) {
+        const int s = j % S;
+        const int sp = (j + S - 1) % S;
+        if (j < nb_max && !(ok = mbar_wait(&k_full[s], (j / S) & 1, ctl))) break;
+        if (j >= 1 && !(ok = mbar_wait(&v_full[sp], ((j - 1) / S) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t colS = L::kColS0 + 128 * t;
+          const uint32_t colO = L::kColO0 + D * t;
+          if (j >= 1 && j - 1 < nb[t]) {
+            if (!(ok = mbar_wait(&p_full[t], (j - 1) & 1, ctl))) break;
+            tc_fence_after();
+            const uint32_t vb = sbase + L::kV + sp * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA; P packed 2 per column
+              const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
+              mma_ts(tmem + colO, tmem + colS + kk * 8, bdesc, idO, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            if (j - 1 == nb[t] - 1) mma_commit(&o_full[t]);
+          }
+          if (j < nb[t]) {
+            const uint32_t qbs = sbase + L::kQ + t * L::kTile;
+            const uint32_t kbs = sbase + L::kK + s * L::kTile;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              const uint64_t adesc = sdesc_sw128(qbs + off, 16384, 1024);
+              const uint64_t bdesc = sdesc_sw128(kbs + off, 16384, 1024);
+              mma_ss(tmem + colS, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&s_full[t]);
+          }
+        }
+        if (!ok) break;
+        if (j < nb_max) mma_commit(&k_empty[s]);
+        if (j >= 1) mma_commit(&v_empty[sp]);
+      }
+      // every MMA issued by this thread has finished before tensor memory is released
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0, ctl);
+    }
+  } else if (warp >= 4) {
+    // ================= softmax warpgroups: one per query tile, one thread per query row
+    const int t = (warp - 4) >> 2;
+    const uint32_t quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int qt0 = q0 + 128 * t;
+    const int qi = qt0 + row;
+    const uint32_t lanes = (quad * 32u) << 16;
+    const uint32_t tS = tmem + lanes + L::kColS0 + 128 * t;
+    const uint32_t tO = tmem + lanes + L::kColO0 + D * t;
+    const float c2 = a.scale_log2;
+    const int n = nb[t];
+    float m_run = -INFINITY;  // running max of scale*log2(e)*s (log2 units)
+    float l_run = 0.f;        // running sum of exp2(. - m_run)
+    float lr_run = 0.f;       // the same sum over the bf16-rounded values (normalises O~)
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = mbar_wait_warp(&s_full[t], j & 1, ctl))) break;
+      tc_fence_after();
+      uint32_t s[128];
+      tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_wait_ld();
+      reg_fence(s);
+      const int k0 = j * 128;
+      const bool masked = (k0 + 128 > kv_len) || (a.causal && k0 == qt0);
+      const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;  // keys < klim are visible
+      float mx = -INFINITY;
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (k0 + c < klim) mx = fmaxf(mx, __uint_as_float(s[c]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      }
+      const float m_tile = mx * c2;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (m_tile > m_run + kRescaleThreshold) {
+        rescale = true;
+        alpha = ex2(m_run - m_tile);  // 0 on the first tile (m_run = -inf)
+        l_run *= alpha;
+        lr_run *= alpha;
+        m_run = m_tile;
+      }
+      const float neg_m = -m_run;
+      float sum = 0.f, sum_r = 0.f;
+      uint32_t p[64];
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float x0 = ex2(fmaf(__uint_as_float(s[2 * c]), c2, neg_m));
+          float x1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), c2, neg_m));
+          x0 = (k0 + 2 * c < klim) ? x0 : 0.f;
+          x1 = (k0 + 2 * c + 1 < klim) ? x1 : 0.f;
+          p[c] = pack_bf16(x0, x1);
+          sum += x0 + x1;
+          if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float x0 = ex2(fmaf(__uint_as_float(s[2 * c]), c2, neg_m));
+          const float x1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), c2, neg_m));
+          p[c] = pack_bf16(x0, x1);
+          sum += x0 + x1;
+          if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
+        }
+      }
+      l_run += sum;
+      lr_run += sum_r;
+      // P over the first 64 columns of S (the MMA issuer reads it as the A operand)
+      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      // O~ *= alpha for rows whose max moved (the previous P V has completed: it was issued
+      // before the S MMA whose completion this warp just observed)
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
+    }
+
+    // ---- epilogue: O = O~ / l -> bf16 -> swizzled smem over Q_t -> TMA store; LSE
+    const bool tile_live = (qt0 < N);
+    if (ok && n > 0) ok = mbar_wait_warp(&o_full[t], 0, ctl);
+    if (tile_live) {  // uniform over the warpgroup
+      if (ok) {
+        tc_fence_after();
+        const float l_o = FA_ROUNDED_SUM ? lr_run : l_run;
+        const float inv_l = (l_o > 0.f) ? 1.f / l_o : 0.f;
+        const uint32_t stage = sbase + L::kQ + t * L::kTile;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (n > 0) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence(o);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
+                              __uint_as_float(o[2 * e + 1]) * inv_l);
+          const uint32_t panel = stage + ((32 * c) / 64) * 16384;
+          const uint32_t g0 = ((32 * c) % 64) / 8;
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            st_shared_v4(panel + sw128_offset(row, g0 + g), pk[4 * g], pk[4 * g + 1],
+                         pk[4 * g + 2], pk[4 * g + 3]);
+        }
+        if (qi < N) {
+          const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+          a.lse[static_cast<size_t>(bh) * N + qi] = lse;
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + t, 128);  // every warp of the group arrives, aborted or not
+      if (quad == 0 && lane == 0 && !*abort_flag) {
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_3d(&tmO, sm + L::kQ + t * L::kTile + c * 16384, c * 64, qt0, bh);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& to, FwdArgs a, cudaStream_t st) {
+  using L = FwdLayout<D>;
+  const uint32_t smem = L::kBytes + 1024;
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  a.smem_bytes = smem;
+  const unsigned grid = static_cast<unsigned>(a.num_qblocks) * static_cast<unsigned>(a.BH);
+  fwd_kernel<D><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t s) {
+  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, a, s);
+  return launch_fwd_d<128>(tq, tk, tv, to, a, s);
+}
+
+}  // namespace fa

@@ -1,0 +1,60 @@
+// Internal interface between the C-ABI layer (fa_api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+constexpr int kTileRows = 128;  // query rows per Q tile and keys per K/V tile
+
+// Forward kernel arguments (tensor maps travel separately as __grid_constant__ parameters).
+struct FwdArgs {
+  int H, N, BH;
+  int num_qblocks;        // 256-row query blocks per (b, h)
+  int causal;
+  float scale_log2;       // scale * log2(e)
+  const int32_t* kv_lens; // device int32[B] or nullptr
+  float* lse;             // [B, H, N] fp32
+  int* status;            // library status word (device)
+  uint64_t timeout_ns;    // limit of a single pipeline wait
+  uint32_t smem_bytes;    // dynamic shared memory actually granted
+};
+
+struct BwdArgs {
+  int H, N, BH;
+  int num_qtiles;         // ceil(N / 128) = padded rows / 128
+  int causal;
+  float scale;            // softmax scale (dK is scaled by it at the end)
+  float scale_log2;       // scale * log2(e)
+  const int32_t* kv_lens;
+  const float* lse2;      // workspace: LSE * log2(e), [BH][Npad], +inf on padded rows
+  const float* delta;     // workspace: D = rowsum(dO o O), [BH][Npad], 0 on padded rows
+  float* dq_acc;          // workspace: dQ accumulator, tile-major (see fa_bwd.cu)
+  int* status;
+  uint64_t timeout_ns;
+  uint32_t smem_bytes;
+};
+
+// Workspace layout (all offsets 256-byte aligned): dq_acc | lse2 | delta
+struct Workspace {
+  size_t dq_acc_off, lse2_off, delta_off, total;
+};
+Workspace workspace_layout(int BH, int N, int d);
+
+// Launchers return cudaSuccess or the launch error.
+cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse,
+                                  int BH, int N, float* lse2, float* delta, float* dq_acc,
+                                  cudaStream_t s);
+cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
+                            cudaStream_t s);
+cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N,
+                                  float scale, cudaStream_t s);
+
+}  // namespace fa

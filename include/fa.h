@@ -1,0 +1,118 @@
+/*
+ * Exact IO-aware attention (forward and backward) for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The operation is exact scaled-dot-product attention, O = softmax(scale * Q K^T) V, computed
+ * tile by tile with online-softmax running statistics so that the N x N score and probability
+ * matrices never reach device memory, and its backward pass, which recomputes P from the
+ * log-sum-exp saved by the forward pass.
+ *   Definition:  "FlashAttention：不减少一次注意力计算，为什么反而更快", section 关键设计一
+ *                (S = QK^T/sqrt(d), P = softmax(S), O = PV);
+ *   recurrence:  "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section
+ *                "FlashAttention-1：分块与在线 softmax", Fig. 4;
+ *   backward:    first page, section 关键设计三 (D_i = dO_i . O_i, dS = P o (dP - D)).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are contiguous [B, H, N, d] bfloat16 (the layout of torch.bfloat16 tensors of
+ *     that shape), row statistics are contiguous [B, H, N] float32.  Every pointer is DEVICE
+ *     memory owned by the caller and must be 16-byte aligned.  The library allocates no
+ *     device memory; the backward pass takes a caller-provided workspace.
+ *   - d (head dimension) is 64 or 128; N >= 1 is any length (no tile multiple needed);
+ *     B * H <= 2^31 - 1.
+ *   - scale < 0 selects the default 1/sqrt(d) (softmax_scale=None in the pages' interface,
+ *     first page, section 使用契约); scale == 0 is allowed.
+ *   - causal != 0 masks key j > query i.  kv_lens (DEVICE int32[B], or NULL for "all N") masks
+ *     keys j >= kv_lens[b] of batch b; values are clamped to [0, N].  A query row with no
+ *     unmasked key gets O = 0, LSE = -inf and zero gradients.
+ *   - stream is a cudaStream_t passed as void*; NULL is the legacy default stream.  Calls are
+ *     asynchronous with respect to the host.
+ *   - Argument errors are returned synchronously before anything is launched.  A launch
+ *     failure returns FA_ERR_CUDA.  A device-side pipeline wait that exceeds its time limit
+ *     ends the kernel cleanly and records FA_ERR_TIMEOUT in a library-owned device status
+ *     word, which fa_get_error() reports.
+ *   - Outputs are fully overwritten; inputs are never modified.
+ */
+#ifndef EXACT_IO_AWARE_FA_H
+#define EXACT_IO_AWARE_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, non-positive size, bad workspace size */
+  FA_ERR_UNSUPPORTED = 2,  /* head dimension other than 64/128, no sm_100-family GPU */
+  FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a kernel launch failed */
+  FA_ERR_TIMEOUT = 4,      /* a device pipeline wait ran past its limit (see fa_get_error) */
+  FA_ERR_WORKSPACE = 5     /* workspace pointer NULL or smaller than fa_bwd_workspace_size() */
+} fa_status;
+
+/*
+ * Forward pass.  Computes, for every (b, h):
+ *   O[b,h]   = softmax(scale * Q[b,h] K[b,h]^T, masked) V[b,h]            [N, d] bf16
+ *   LSE[b,h] = log sum_j exp(scale * q_i . k_j)  (natural log, masked)     [N]    fp32
+ * Q, K, V: inputs [B,H,N,d] bf16.  O: output [B,H,N,d] bf16.  LSE: output [B,H,N] fp32.
+ * Cite: first page, 关键设计一/二 (tiling, online softmax, L = m + log l saved for backward).
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int N, int d, int causal, float scale,
+                 const int32_t* kv_lens, void* stream);
+
+/*
+ * Bytes of workspace fa_bwd needs for these sizes: a float32 dQ accumulator plus the per-row
+ * statistics D = rowsum(dO o O) and LSE * log2(e), each padded to a multiple of 128 rows per
+ * (b, h).  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass: dQ, dK, dV (all [B,H,N,d] bf16 outputs) of L with dL/dO = dO, given the
+ * forward inputs Q, K, V, its outputs O and LSE, and the same B, H, N, d, causal, scale and
+ * kv_lens.  Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert in that order on
+ * `stream`.  workspace: DEVICE memory of at least fa_bwd_workspace_size() bytes, 256-byte
+ * aligned, owned by the caller, contents on entry irrelevant.
+ * Cite: first page, 关键设计三 (recomputation of S_ij, P_ij from the saved statistic;
+ * dV += P^T dO, dQ += dS K, dK += dS^T Q).
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV,
+                 int B, int H, int N, int d, int causal, float scale,
+                 const int32_t* kv_lens, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The three stages of fa_bwd, exported so that each can be launched (and timed) on its own.
+ * They must run in this order on one stream with the same arguments and workspace.
+ *  fa_bwd_preprocess: D_i = sum_k dO_ik O_ik, LSE_i * log2(e) into the workspace, and zeroes
+ *                     the dQ accumulator (first page, 关键设计三, D_i = dO_i^T O_i).
+ *  fa_bwd_dkdv:       one pass over the query tiles per key tile: recomputes P^T from LSE,
+ *                     writes dK, dV and adds dS K into the dQ accumulator with float32
+ *                     atomics (non-deterministic in the last bits).
+ *  fa_bwd_dq_convert: dQ = bf16(scale * accumulator).
+ */
+fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE,
+                            int B, int H, int N, int d,
+                            void* workspace, size_t workspace_bytes, void* stream);
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO,
+                      void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
+                      const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                      void* stream);
+fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, returns the first device-side error recorded since the previous call
+ * (FA_OK if none) and clears it.  A pending CUDA error on the stream gives FA_ERR_CUDA.
+ */
+fa_status fa_get_error(void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* fa_status_string(fa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_IO_AWARE_FA_H */

@@ -123,11 +123,14 @@ def row_statistics(q, k, v, do, scale, causal=False, kv_len=None, rows=None):
     return out
 
 
-def key_gradients(q, k, v, do, scale, lse, d_row, causal=False, kv_len=None, cols=None):
-    """dK[cols], dV[cols] from the per-row statistics LSE and D of *all* query rows.
+def key_gradients(q, k, v, do, scale, lse, d_row, causal=False, kv_len=None, cols=None,
+                  rows=None):
+    """dK[cols], dV[cols] as sums over the query rows ``rows`` (default: all rows).
 
     dV_j = sum_i P_ij dO_i,  dK_j = scale * sum_i dS_ij Q_i,  with P_ij = exp(s_ij - LSE_i) and
-    dS_ij = P_ij (dP_ij - D_i), dP_ij = dO_i . V_j.
+    dS_ij = P_ij (dP_ij - D_i), dP_ij = dO_i . V_j.  ``lse`` and ``d_row`` are the statistics of
+    the rows summed over (as returned by ``row_statistics`` for the same rows); summing the
+    results over a partition of the rows gives the full gradients.
     """
     q = _f64(q)
     k = _f64(k)
@@ -135,11 +138,14 @@ def key_gradients(q, k, v, do, scale, lse, d_row, causal=False, kv_len=None, col
     do = _f64(do)
     n_q, n_k = q.shape[0], k.shape[0]
     cols = np.arange(n_k) if cols is None else np.asarray(cols, dtype=np.int64)
-    # scores of every query row against the selected keys, masked like masked_scores
+    rows = np.arange(n_q) if rows is None else np.asarray(rows, dtype=np.int64)
+    q = q[rows]
+    do = do[rows]
+    # scores of the summed query rows against the selected keys, masked like masked_scores
     s = float(scale) * (q @ k[cols].T)
     masked = np.zeros(s.shape, dtype=bool)
     if causal:
-        masked |= cols[None, :] > np.arange(n_q)[:, None]
+        masked |= cols[None, :] > rows[:, None]
     if kv_len is not None:
         masked |= cols[None, :] >= int(kv_len)
     s[masked] = -np.inf

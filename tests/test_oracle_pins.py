@@ -252,3 +252,18 @@ def test_against_torch_cpu_attention_float64(causal, kv_len):
     assert np.max(np.abs(o.detach().numpy() - st["O"])) < 1e-12
     for name, t in (("dQ", tq), ("dK", tk), ("dV", tv)):
         assert np.max(np.abs(t.grad.numpy() - st[name])) < 1e-11, name
+
+
+def test_key_gradients_sum_over_row_partition():
+    n, d = 12, 3
+    q, k, v, do = (_rand(n, d, s) for s in (49, 50, 51, 52))
+    st = oracle.attention_backward(q, k, v, do, 0.6, True, 10)
+    parts = [np.arange(0, 5), np.arange(5, 12)]
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for rows in parts:
+        kg = oracle.key_gradients(q, k, v, do, 0.6, st["LSE"][rows], st["D"][rows], True, 10,
+                                  rows=rows)
+        dk += kg["dK"]
+        dv += kg["dV"]
+    assert np.max(np.abs(dk - st["dK"])) < 1e-13 and np.max(np.abs(dv - st["dV"])) < 1e-13

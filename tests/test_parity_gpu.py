@@ -1,0 +1,122 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element by element.
+
+Small cases run every (b, h) slice and cover several tiles plus a ragged tail; the five
+synthetic workloads run at full size in the same launch configuration the benchmark times and
+compare seeded (b, h) slices in full.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from exact_io_aware_fwd_gb300.workloads import WORKLOADS, make_inputs, sample_slices, workload_inputs
+
+from parity import check_case, f64, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import exact_io_aware_fwd_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+
+
+SMALL = [
+    # B, H, N, d, causal, kv range, sigma_qk, scale
+    (1, 1, 128, 64, False, None, 1.0, None),
+    (1, 1, 128, 128, True, None, 1.0, None),
+    (2, 2, 300, 64, False, None, 1.0, None),
+    (2, 2, 300, 128, True, None, 1.0, None),
+    (1, 3, 256, 64, True, None, 1.0, None),
+    (2, 1, 517, 128, False, (300, 517), 3.0, None),
+    (2, 2, 389, 64, True, (1, 389), 2.0, None),
+    (1, 2, 640, 128, False, None, 3.0, 0.05),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"B{c[0]}H{c[1]}N{c[2]}d{c[3]}{'c' if c[4] else ''}")
+def test_small_cases(case):
+    B, H, N, d, causal, kvr, sqk, scale = case
+    q, k, v, do, kv = make_inputs(B, H, N, d, seed=100 + N + d, sigma_qk=sqk, kv_len_range=kvr)
+    check_case(q, k, v, do, causal, scale, kv, label=str(case))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 2, 5, 127, 129, 255, 257])
+def test_edge_lengths(N, d):
+    q, k, v, do, _ = make_inputs(1, 2, N, d, seed=7 * N + d)
+    # With a handful of keys the gradients' relative norm is taken over a few numbers, and
+    # dS = P (dP - D) with D = dO . O computed from the bf16-rounded O (the identity of the
+    # backward pass) can cancel: a relative error of 2^-8 |dO||O| in D is not averaged out.
+    # Below 16 keys the gradient bound is therefore 5e-2 instead of 2e-2.
+    grad_tol = 5e-2 if N < 16 else None
+    for causal in (False, True):
+        check_case(q, k, v, do, causal, None, None, label=f"N={N} d={d} causal={causal}",
+                   grad_tol=grad_tol)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_zero_scale_gives_mean_of_values(d):
+    q, k, v, do, _ = make_inputs(1, 1, 200, d, seed=3)
+    out, _ = check_case(q, k, v, do, False, 0.0, None, label="scale=0")
+    mean = v[0, 0].double().mean(dim=0).numpy()
+    assert np.max(np.abs(f64(out["O"][0, 0]) - mean)) < 1e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_key_length_one_and_zero(d):
+    q, k, v, do, _ = make_inputs(3, 1, 300, d, seed=11)
+    kv = torch.tensor([1, 0, 300], dtype=torch.int32)
+    out, _ = check_case(q, k, v, do, False, None, kv, label="kv 1/0/300")
+    # kv_len = 1: every row attends to key 0 only
+    assert np.max(np.abs(f64(out["O"][0, 0]) - v[0, 0, 0].double().numpy())) < 1e-2
+    # kv_len = 0: no key at all
+    assert torch.all(out["O"][1] == 0) and torch.all(torch.isneginf(out["LSE"][1]))
+    for name in ("dQ", "dK", "dV"):
+        assert torch.all(out[name][1] == 0)
+
+
+def test_causal_first_row_is_first_value():
+    q, k, v, do, _ = make_inputs(1, 2, 1000, 128, seed=5)
+    out = run_gpu(q, k, v, do, True, None, None, with_bwd=False)
+    first = f64(out["O"][0, :, 0])
+    assert np.max(np.abs(first - v[0, :, 0].double().numpy())) < 1e-2
+
+
+def test_outputs_do_not_write_past_n():
+    """Rows past N belong to the next (b, h): a canary after the last row must survive."""
+    import exact_io_aware_fwd_gb300 as fa
+
+    B, H, N, d = 1, 1, 200, 128
+    q, k, v, do, _ = make_inputs(B, H, N, d, seed=9)
+    dev = torch.device("cuda:0")
+    extra = 300
+    outs = {}
+    for name in ("O", "dQ", "dK", "dV"):
+        buf = torch.full((N + extra, d), 7.0, dtype=torch.bfloat16, device=dev)
+        outs[name] = buf
+    view = lambda buf: buf[:N].view(B, H, N, d)  # noqa: E731
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    lse_buf = torch.full((N + extra,), 7.0, device=dev)
+    o, lse = fa.fa_fwd(qd, kd, vd, out=view(outs["O"]), lse=lse_buf[:N].view(B, H, N))
+    fa.fa_bwd(qd, kd, vd, o, dod, lse, dq=view(outs["dQ"]), dk=view(outs["dK"]), dv=view(outs["dV"]))
+    assert fa.fa_get_error() == fa.FA_OK
+    for name, buf in outs.items():
+        assert torch.all(buf[N:] == 7.0), name
+    assert torch.all(lse_buf[N:] == 7.0)
+
+
+def test_forward_is_deterministic():
+    q, k, v, do, _ = make_inputs(2, 2, 700, 128, seed=13)
+    a = run_gpu(q, k, v, do, True, None, None, with_bwd=False)
+    b = run_gpu(q, k, v, do, True, None, None, with_bwd=False)
+    assert torch.equal(a["O"], b["O"]) and torch.equal(a["LSE"], b["LSE"])
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=lambda w: w.name)
+def test_workloads_full_size(w):
+    q, k, v, do, kv = workload_inputs(w)
+    check_case(q, k, v, do, w.causal, w.scale, kv, slices=sample_slices(w), label=w.name)
