@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     fa_bwd,
     fa_bwd_dkdv,
     fa_bwd_dq_convert,
+    fa_bwd_noalloc,
     fa_bwd_preprocess,
     fa_bwd_workspace_size,
     fa_fwd,

@@ -30,6 +30,7 @@ EXPORTED = [
     "fa_bwd_preprocess",
     "fa_bwd_dkdv",
     "fa_bwd_dq_convert",
+    "fa_bwd_noalloc",
     "fa_get_error",
     "fa_status_string",
 ]
@@ -65,6 +66,8 @@ def load_library(path: str | None = None):
     lib.fa_bwd_dkdv.restype = i
     lib.fa_bwd_dq_convert.argtypes = [vp, i, i, i, i, f, vp, sz, vp]
     lib.fa_bwd_dq_convert.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_get_error.argtypes = [vp]
     lib.fa_get_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -181,6 +184,23 @@ def fa_bwd_dq_convert(dq, workspace, scale=None, stream=None):
     st = load_library().fa_bwd_dq_convert(_ptr(dq), B, H, N, d, _scale(scale), _ptr(workspace),
                                           workspace.numel(), _stream(stream))
     _check(st, "fa_bwd_dq_convert")
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dq=None,
+                   dk=None, dv=None, stream=None):
+    """fa_bwd with the library's static workspace, for callers that cannot allocate device
+    memory (see include/fa.h); calls that overlap on the GPU must be serialised."""
+    B, H, N, d = _check_qkv(q, k, v, o, do)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                       _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                       int(bool(causal)), _scale(scale), _ptr(kv),
+                                       _stream(stream))
+    _check(st, "fa_bwd_noalloc")
+    return dq, dk, dv
 
 
 def fa_get_error(stream=None) -> int:

@@ -103,6 +103,26 @@ fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale,
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd for callers that cannot allocate device memory.  The pages have no counterpart: this
+ * entry point exists for callers with no device allocator to take the backward workspace from
+ * (code running where cudaMalloc is forbidden or unsafe, such as host callbacks or allocator
+ * hooks, plugins whose host framework owns every allocation, or C callers without one).
+ * Arguments and results are those of fa_bwd without the workspace: the workspace is a 64 MiB
+ * static device array inside the library, held by every GPU that loads the library until the
+ * process exits.  Sizes with fa_bwd_workspace_size(B, H, N, d) > 64 MiB return
+ * FA_ERR_WORKSPACE before anything is launched (at d = 128 that is about 129,000 padded rows
+ * B * H * roundup(N, 128); at d = 64 about 254,000).  Nothing is allocated.  The first call on
+ * each device looks up the array's device address with that device current; make it before
+ * any stream capture.  All calls share the array: calls that overlap on the GPU race and must
+ * be serialised by the caller.  Every part of the array a call reads is first rewritten by the
+ * same call (the dQ accumulator is zeroed), so earlier contents never affect a result.
+ */
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                         int B, int H, int N, int d, int causal, float scale,
+                         const int32_t* kv_lens, void* stream);
+
+/*
  * Synchronises `stream`, returns the first device-side error recorded since the previous call
  * (FA_OK if none) and clears it.  A pending CUDA error on the stream gives FA_ERR_CUDA.
  */
