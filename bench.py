@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="override H (smaller profiling captures of the same shape); the line "
+                         "is then not the headline measurement")
     return ap.parse_args()
 
 
@@ -391,6 +394,10 @@ def run_ours(args, w, world, rank, local):
 def main():
     args = parse()
     w = BY_NAME[args.workload]
+    if args.heads is not None:
+        from dataclasses import replace
+
+        w = replace(w, H=args.heads, name=f"{w.name}[H={args.heads}]")
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, w, world, rank)

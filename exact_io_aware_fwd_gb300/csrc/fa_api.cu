@@ -6,7 +6,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/fa.h"
+#include "fa.h"
 #include "fa_internal.h"
 
 namespace {

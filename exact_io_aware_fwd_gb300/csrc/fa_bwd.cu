@@ -12,7 +12,11 @@
 //                  D = 0 and +inf, which makes their recomputed P exactly 0), and zeroes the
 //                  float32 dQ accumulator.
 //  bwd_dkdv        one CTA per (b, h, 128-key tile j); dK_j and dV_j accumulate in tensor memory
-//                  over the query tiles i (causal: i >= j only).  Per query tile:
+//                  over the query tiles i (causal: i >= j only).  16 warps: TMA producer, MMA
+//                  issuer, two warpgroups that each handle 64 of the 128 query columns of every
+//                  key row for P and dS (two warps per SM sub-partition hide each other's
+//                  tensor-memory and shared-memory latency), and a warpgroup that drains dQ_i
+//                  and writes dK, dV at the end.  Per query tile:
 //                    S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (tcgen05, both operands in smem)
 //                    P^T = exp2(S^T * scale * log2 e - LSE_i * log2 e), written back over S^T
 //                    dS^T = P^T o (dP^T - D_i), written back over dP^T and to smem
@@ -149,13 +153,21 @@ struct BwdLayout {
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4;
-  // TMEM columns
+  // TMEM columns.  S^T (fp32) in [0, 128); P^T packed as bf16 pairs over the first half of each
+  // 64-query half's own columns: queries 64h..64h+63 -> columns [64h, 64h + 32).  dP^T (fp32) in
+  // [128, 256), dS^T packed the same way at 128 + [64h, 64h + 32); dQ_i (fp32, D columns) is
+  // accumulated over [128, 128 + D) once dK += dS^T Q has consumed dS^T.
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
   static constexpr uint32_t kTmemCols = 512;
 };
 
+// Packed bf16 column of the 16-query k-step kk (0..7) inside the S^T or dP^T region.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+constexpr int kBwdThreads = 512;
+
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmdK,
@@ -190,10 +202,11 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
 
-  // ---- work item: key tile j (small j first: with a causal mask they have the most work)
+  // ---- work item: head-major (one or two heads' Q, dO and dQ accumulator live in L2 at a
+  // time); within a head key tile 0 first (with a causal mask the lowest tiles have most work)
   const int lin = blockIdx.x;
-  const int bh = lin % a.BH;
-  const int j = lin / a.BH;
+  const int bh = lin / a.num_qtiles;
+  const int j = lin % a.num_qtiles;
   const int b = bh / a.H;
   const int N = a.N;
   const int nqt = a.num_qtiles;
@@ -206,9 +219,12 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
     for (int k = 0; k < L::kNumBars; ++k) {
-      // P, dS and the dQ release are signalled by the four warps of a warpgroup
-      const bool per_warp = (&bars[k] == p_full) || (&bars[k] == ds_full) || (&bars[k] == dq_empty);
-      mbar_init(&bars[k], per_warp ? 4 : 1);
+      // P and dS are signalled by the eight warps of the two P/dS warpgroups, the dQ release by
+      // the four drain warps
+      uint32_t count = 1;
+      if (&bars[k] == p_full || &bars[k] == ds_full) count = 8;
+      if (&bars[k] == dq_empty) count = 4;
+      mbar_init(&bars[k], count);
     }
     fence_mbar_init();
     tma_prefetch_desc(&tmQ);
@@ -269,98 +285,140 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);    // dV, dK: A in TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, D, true, true);      // dQ: A = dS MN-major, B MN-major
       const uint32_t kb = sbase + L::kK, vb = sbase + L::kV, dsb = sbase + L::kDS;
-      bool ok = mbar_wait(kv_full, 0, ctl);
-      for (int it = 0; ok && it < nI; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        const uint32_t qb = sbase + L::kQ + s * L::kTile;
-        const uint32_t dob = sbase + L::kDO + s * L::kTile;
-        if (!(ok = mbar_wait(&q_full[s], ph, ctl))) break;
-        tc_fence_after();
+      // Issue order (software-pipelined over query tiles): S(0), dP(0), dV(0), S(1), then per
+      // tile i: dK(i), dQ(i) | dV(i+1), dP(i+1) | S(i+2).  The tensor pipe always has the next
+      // tile's work queued while the P/dS warpgroups compute, and dV(i+1) covers the drain of
+      // dQ(i) that dP(i+1) waits for.  Q_i is released after dK(i), dO_i after dV(i).
+      auto issue_S = [&](int it) {  // S^T = K_j Q_i^T
+        const uint32_t qb = sbase + L::kQ + (it & 1) * L::kTile;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // S^T = K_j Q_i^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + L::kColS, sdesc_sw128(kb + off, 16384, 1024),
                  sdesc_sw128(qb + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(s_full);
-        if (!(ok = mbar_wait(&do_full[s], ph, ctl))) break;
-        if (it > 0 && !(ok = mbar_wait(dq_empty, (it - 1) & 1, ctl))) break;
-        tc_fence_after();
+      };
+      auto issue_dP = [&](int it) {  // dP^T = V_j dO_i^T
+        const uint32_t dob = sbase + L::kDO + (it & 1) * L::kTile;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {  // dP^T = V_j dO_i^T
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
           mma_ss(tmem + L::kColDP, sdesc_sw128(vb + off, 16384, 1024),
                  sdesc_sw128(dob + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
         }
         mma_commit(dp_full);
-        if (!(ok = mbar_wait(p_full, it & 1, ctl))) break;
-        tc_fence_after();
+      };
+      auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA)
+        const uint32_t dob = sbase + L::kDO + (it & 1) * L::kTile;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += P^T dO_i   (128 queries, 16 per MMA)
-          mma_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8, sdesc_sw128(dob + kk * 2048, 16384, 1024),
-                 idKV, (it > 0 || kk > 0) ? 1u : 0u);
-        if (!(ok = mbar_wait(ds_full, it & 1, ctl))) break;
-        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + L::kColDV, tmem + L::kColS + packed_col(kk),
+                 sdesc_sw128(dob + kk * 2048, 16384, 1024), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&do_empty[it & 1]);
+      };
+      auto issue_dK_dQ = [&](int it) {
+        const uint32_t qb = sbase + L::kQ + (it & 1) * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + L::kColDK, tmem + L::kColDP + kk * 8, sdesc_sw128(qb + kk * 2048, 16384, 1024),
-                 idKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kColDK, tmem + L::kColDP + packed_col(kk),
+                 sdesc_sw128(qb + kk * 2048, 16384, 1024), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&q_empty[it & 1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
           mma_ss(tmem + L::kColDP, sdesc_sw128(dsb + kk * 2048, 16384, 1024),
                  sdesc_sw128(kb + kk * 2048, 16384, 1024), idQ, kk > 0 ? 1u : 0u);
         mma_commit(dq_full);
-        mma_commit(&q_empty[s]);
-        mma_commit(&do_empty[s]);
+      };
+      auto wait_q = [&](int it) { return mbar_wait(&q_full[it & 1], (it >> 1) & 1, ctl); };
+      auto wait_do = [&](int it) { return mbar_wait(&do_full[it & 1], (it >> 1) & 1, ctl); };
+
+      bool ok = mbar_wait(kv_full, 0, ctl) && wait_q(0);
+      if (ok) {
+        tc_fence_after();
+        issue_S(0);
+        ok = wait_do(0);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dP(0);
+        ok = mbar_wait(p_full, 0, ctl);
+      }
+      if (ok) {
+        tc_fence_after();
+        issue_dV(0);
+        if (nI > 1 && (ok = wait_q(1))) {
+          tc_fence_after();
+          issue_S(1);
+        }
+      }
+      for (int it = 0; ok && it < nI; ++it) {
+        if (!(ok = mbar_wait(ds_full, it & 1, ctl))) break;
+        tc_fence_after();
+        issue_dK_dQ(it);
+        if (it + 1 < nI) {
+          if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl))) break;
+          tc_fence_after();
+          issue_dV(it + 1);
+          if (!(ok = wait_do(it + 1) && mbar_wait(dq_empty, it & 1, ctl))) break;
+          tc_fence_after();
+          issue_dP(it + 1);
+          if (it + 2 < nI) {
+            if (!(ok = wait_q(it + 2))) break;
+            tc_fence_after();
+            issue_S(it + 2);
+          }
+        }
       }
       if (ok) mma_commit(dkdv_full);
       mma_commit(mma_done);
       drain_wait(mma_done, 0, ctl);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ================= P and dS: one thread per key row of the tile
+  } else if (warp >= 4 && warp < 12) {
+    // ================= P and dS: one thread per key row, one warpgroup per 64-query half
     const uint32_t quad = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int r = quad * 32 + lane;
     const int key = j * 128 + r;
     const bool row_live = key < kv_len;
     const uint32_t lanes = (quad * 32u) << 16;
-    const uint32_t tS = tmem + lanes + L::kColS;
-    const uint32_t tDP = tmem + lanes + L::kColDP;
+    const uint32_t tS = tmem + lanes + L::kColS + 64 * half;
+    const uint32_t tDP = tmem + lanes + L::kColDP + 64 * half;
     const float c2 = a.scale_log2;
-    const uint32_t dsb = sbase + L::kDS;
+    const uint32_t dsb = sbase + L::kDS + half * 16384;
     for (int it = 0; it < nI; ++it) {
       const int i = i0 + it, s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
       if (!mbar_wait_warp(&q_full[s], ph, ctl)) break;  // LSE and D of this tile are in smem
       if (!mbar_wait_warp(s_full, it & 1, ctl)) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512);
-      const float* dl = reinterpret_cast<const float*>(sm + L::kDelta + s * 512);
+      const float* lse2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512) + 64 * half;
+      const float* dl = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + 64 * half;
       const bool diag = a.causal && (i == j);
-      uint32_t p[64];
+      uint32_t p[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t sv[32];
         tmem_ld32(tS + 32 * c, sv);
         tmem_wait_ld();
         reg_fence(sv);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = 32 * c + 2 * e;
-          const float2 l2 = *reinterpret_cast<const float2*>(lse2 + q);
-          float x0 = ex2(fmaf(__uint_as_float(sv[2 * e]), c2, -l2.x));
-          float x1 = ex2(fmaf(__uint_as_float(sv[2 * e + 1]), c2, -l2.y));
-          if (diag) {
-            x0 = (r <= q) ? x0 : 0.f;  // key j*128+r > query i*128+q is masked
-            x1 = (r <= q + 1) ? x1 : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const int ql = 32 * c + 4 * e;  // query within this half
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + ql);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          float x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            x[u] = ex2(fmaf(__uint_as_float(sv[4 * e + u]), c2, -lv[u]));
+            if (diag) x[u] = (r <= 64 * half + ql + u) ? x[u] : 0.f;  // key > query: masked
+            if (!row_live) x[u] = 0.f;
           }
-          if (!row_live) x0 = x1 = 0.f;
-          p[16 * c + e] = pack_bf16(x0, x1);
+          p[16 * c + 2 * e] = pack_bf16(x[0], x[1]);
+          p[16 * c + 2 * e + 1] = pack_bf16(x[2], x[3]);
         }
       }
-      tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-      tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+      tmem_st32(tS, p);  // P^T over this half's first 32 columns (all of its S^T was read)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -369,28 +427,28 @@ __global__ void __launch_bounds__(384, 1)
       if (!mbar_wait_warp(dp_full, it & 1, ctl)) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t dv[32];
         tmem_ld32(tDP + 32 * c, dv);
         tmem_wait_ld();
         reg_fence(dv);
         uint32_t ds[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = 32 * c + 2 * e;
-          const float2 dd = *reinterpret_cast<const float2*>(dl + q);
-          const float p0 = bf16_lo(p[16 * c + e]), p1 = bf16_hi(p[16 * c + e]);
-          ds[e] = pack_bf16(p0 * (__uint_as_float(dv[2 * e]) - dd.x),
-                            p1 * (__uint_as_float(dv[2 * e + 1]) - dd.y));
+        for (int e = 0; e < 8; ++e) {
+          const int ql = 32 * c + 4 * e;
+          const float4 d4 = *reinterpret_cast<const float4*>(dl + ql);
+          const uint32_t pa = p[16 * c + 2 * e], pb = p[16 * c + 2 * e + 1];
+          ds[2 * e] = pack_bf16(bf16_lo(pa) * (__uint_as_float(dv[4 * e]) - d4.x),
+                                bf16_hi(pa) * (__uint_as_float(dv[4 * e + 1]) - d4.y));
+          ds[2 * e + 1] = pack_bf16(bf16_lo(pb) * (__uint_as_float(dv[4 * e + 2]) - d4.z),
+                                    bf16_hi(pb) * (__uint_as_float(dv[4 * e + 3]) - d4.w));
         }
-        // dS^T packed over the dP^T columns already read (A operand of dK += dS^T Q)
+        // dS^T packed over dP^T columns this half has already read (A operand of dK += dS^T Q)
         tmem_st16(tDP + 16 * c, ds);
         // and to smem as [key row][query], 128-byte swizzled (A operand of dQ = dS K)
-        const uint32_t panel = dsb + (c >> 1) * 16384;
-        const uint32_t g0 = (c & 1) * 4;
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          st_shared_v4(panel + sw128_offset(r, g0 + g), ds[4 * g], ds[4 * g + 1], ds[4 * g + 2],
+          st_shared_v4(dsb + sw128_offset(r, 4 * c + g), ds[4 * g], ds[4 * g + 1], ds[4 * g + 2],
                        ds[4 * g + 3]);
       }
       tmem_wait_st();
@@ -399,7 +457,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ================= dQ reduction and the dK / dV epilogue: one thread per row
     const uint32_t quad = warp & 3;
     const int r = quad * 32 + lane;
@@ -411,22 +469,29 @@ __global__ void __launch_bounds__(384, 1)
       if (!(ok = mbar_wait_warp(dq_full, it & 1, ctl))) break;
       tc_fence_after();
       float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tDP + 32 * c, v);
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {  // 64 columns per round: two loads, then the atomics
+        uint32_t va[32], vb[32];
+        tmem_ld32(tDP + 64 * c, va);
+        tmem_ld32(tDP + 64 * c + 32, vb);
         tmem_wait_ld();
-        reg_fence(v);
-        if (c == D / 32 - 1) {  // tensor memory fully read: release it before the reductions
+        reg_fence(va);
+        reg_fence(vb);
+        if (c == D / 64 - 1) {  // tensor memory fully read: release it before the reductions
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(dq_empty);
         }
 #pragma unroll
         for (int g = 0; g < 8; ++g)
-          red_add_v4(tile + ((8 * c + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
-                     __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
-                     __uint_as_float(v[4 * g + 3]));
+          red_add_v4(tile + ((16 * c + g) * 128 + r) * 4, __uint_as_float(va[4 * g]),
+                     __uint_as_float(va[4 * g + 1]), __uint_as_float(va[4 * g + 2]),
+                     __uint_as_float(va[4 * g + 3]));
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          red_add_v4(tile + ((16 * c + 8 + g) * 128 + r) * 4, __uint_as_float(vb[4 * g]),
+                     __uint_as_float(vb[4 * g + 1]), __uint_as_float(vb[4 * g + 2]),
+                     __uint_as_float(vb[4 * g + 3]));
       }
     }
     if (ok && nI > 0) ok = mbar_wait_warp(dkdv_full, 0, ctl);
@@ -523,7 +588,7 @@ cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dkdv_kernel<D><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
   return cudaGetLastError();
 }
 }  // namespace

@@ -111,7 +111,9 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
 
-  // ---- work item: heaviest causal blocks first, all heads of a block level together
+  // ---- work item: the heaviest causal blocks of all heads first, so that every wave holds CTAs
+  // of similar length and the light ones fill the tail (measured on GB300: 6% faster than a
+  // head-major order on the long causal case, whose better L2 locality does not pay here)
   const int lin = blockIdx.x;
   const int bh = lin % a.BH;
   const int qb = a.causal ? (a.num_qblocks - 1 - lin / a.BH) : (lin / a.BH);
@@ -272,15 +274,19 @@ __global__ void __launch_bounds__(384, 1)
       const int k0 = j * 128;
       const bool masked = (k0 + 128 > kv_len) || (a.causal && k0 == qt0);
       const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;  // keys < klim are visible
-      float mx = -INFINITY;
+      // row max as 4 independent chains (a single chain is 128 dependent FMNMX)
+      float mxv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mxv[e] = -INFINITY;
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
-          if (k0 + c < klim) mx = fmaxf(mx, __uint_as_float(s[c]));
+          if (k0 + c < klim) mxv[c & 3] = fmaxf(mxv[c & 3], __uint_as_float(s[c]));
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+        for (int c = 0; c < 128; ++c) mxv[c & 3] = fmaxf(mxv[c & 3], __uint_as_float(s[c]));
       }
+      const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
       const float m_tile = mx * c2;
       float alpha = 1.f;
       bool rescale = false;
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(384, 1)
         m_run = m_tile;
       }
       const float neg_m = -m_run;
-      float sum = 0.f, sum_r = 0.f;
+      float sumv[4] = {0.f, 0.f, 0.f, 0.f}, sum_r = 0.f;
       uint32_t p[64];
       if (masked) {
 #pragma unroll
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(384, 1)
           x0 = (k0 + 2 * c < klim) ? x0 : 0.f;
           x1 = (k0 + 2 * c + 1 < klim) ? x1 : 0.f;
           p[c] = pack_bf16(x0, x1);
-          sum += x0 + x1;
+          sumv[c & 3] += x0 + x1;
           if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
         }
       } else {
@@ -311,11 +317,11 @@ __global__ void __launch_bounds__(384, 1)
           const float x0 = ex2(fmaf(__uint_as_float(s[2 * c]), c2, neg_m));
           const float x1 = ex2(fmaf(__uint_as_float(s[2 * c + 1]), c2, neg_m));
           p[c] = pack_bf16(x0, x1);
-          sum += x0 + x1;
+          sumv[c & 3] += x0 + x1;
           if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
         }
       }
-      l_run += sum;
+      l_run += (sumv[0] + sumv[1]) + (sumv[2] + sumv[3]);
       lr_run += sum_r;
       // P over the first 64 columns of S (the MMA issuer reads it as the A operand)
       tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));

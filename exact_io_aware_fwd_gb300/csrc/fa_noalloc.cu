@@ -23,7 +23,7 @@
 //  * the first call on each device performs the address lookup; make it before any stream capture.
 #include <mutex>
 
-#include "../../include/fa.h"
+#include "fa.h"
 #include "fa_internal.h"
 
 namespace {
