@@ -165,8 +165,8 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE, int
   const fa::Workspace w = fa::workspace_layout(BH, N, d);
   char* ws = static_cast<char*>(workspace);
   cudaError_t e = fa::launch_bwd_preprocess(
-      d, O, dO, LSE, BH, N, reinterpret_cast<float*>(ws + w.lse2_off),
-      reinterpret_cast<float*>(ws + w.delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
+      d, O, dO, LSE, BH, N, reinterpret_cast<float*>(ws + w.neg_lse2_off),
+      reinterpret_cast<float*>(ws + w.neg_delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -203,8 +203,8 @@ fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* d
   a.scale = resolve_scale(scale, d);
   a.scale_log2 = a.scale * kLog2e;
   a.kv_lens = kv_lens;
-  a.lse2 = reinterpret_cast<const float*>(ws + w.lse2_off);
-  a.delta = reinterpret_cast<const float*>(ws + w.delta_off);
+  a.neg_lse2 = reinterpret_cast<const float*>(ws + w.neg_lse2_off);
+  a.neg_delta = reinterpret_cast<const float*>(ws + w.neg_delta_off);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
   a.status = status;
   a.timeout_ns = wait_timeout_ns();

@@ -8,9 +8,10 @@
 // (with the softmax scale applied to dK and dQ by the chain rule through S = scale * Q K^T).
 //
 // Kernels:
-//  bwd_preprocess  D = rowsum(dO o O) and LSE * log2(e) into the workspace (padded rows get
-//                  D = 0 and +inf, which makes their recomputed P exactly 0), and zeroes the
-//                  float32 dQ accumulator.
+//  bwd_preprocess  -D = -rowsum(dO o O) and -LSE * log2(e) into the workspace (negated so that
+//                  P and dP - D are single packed FMA / add instructions; padded rows get 0 and
+//                  -inf, which makes their recomputed P exactly 0), and zeroes the float32 dQ
+//                  accumulator.
 //  bwd_dkdv        one CTA per (b, h, 128-key tile j); dK_j and dV_j accumulate in tensor memory
 //                  over the query tiles i (causal: i >= j only).  16 warps: TMA producer, MMA
 //                  issuer, two warpgroups that each handle 64 of the 128 query columns of every
@@ -44,9 +45,9 @@ Workspace workspace_layout(int BH, int N, int d) {
   const size_t npad = static_cast<size_t>((N + kTileRows - 1) / kTileRows) * kTileRows;
   Workspace w;
   w.dq_acc_off = 0;
-  w.lse2_off = up(static_cast<size_t>(BH) * npad * d * sizeof(float));
-  w.delta_off = w.lse2_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
-  w.total = w.delta_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  w.neg_lse2_off = up(static_cast<size_t>(BH) * npad * d * sizeof(float));
+  w.neg_delta_off = w.neg_lse2_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  w.total = w.neg_delta_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
   return w;
 }
 
@@ -71,8 +72,8 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
                                                              const __nv_bfloat16* __restrict__ dO,
                                                              const float* __restrict__ lse, int N,
-                                                             int nqt, float* __restrict__ lse2,
-                                                             float* __restrict__ delta,
+                                                             int nqt, float* __restrict__ neg_lse2,
+                                                             float* __restrict__ neg_delta,
                                                              float* __restrict__ dq_acc) {
   constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
   constexpr int RPW = 32 / G;  // rows per warp per pass
@@ -102,8 +103,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
         const float l = __ldg(lse + static_cast<size_t>(bh) * N + q);
         l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;  // a row with no key: P must be 0
       }
-      lse2[idx] = l2;
-      delta[idx] = (q < N) ? acc : 0.f;
+      neg_lse2[idx] = -l2;
+      neg_delta[idx] = (q < N) ? -acc : 0.f;
     }
   }
   float4* t = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D);
@@ -261,8 +262,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(sm + L::kQ + s * L::kTile + c * 16384, &tmQ, &q_full[s], c * 64, i * 128, bh);
         const size_t srow = static_cast<size_t>(bh) * npad + i * 128;
-        bulk_load(sm + L::kLse + s * 512, a.lse2 + srow, 512, &q_full[s]);
-        bulk_load(sm + L::kDelta + s * 512, a.delta + srow, 512, &q_full[s]);
+        bulk_load(sm + L::kLse + s * 512, a.neg_lse2 + srow, 512, &q_full[s]);
+        bulk_load(sm + L::kDelta + s * 512, a.neg_delta + srow, 512, &q_full[s]);
         nq = it + 1;
         if (!mbar_wait(&do_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&do_full[s], L::kTile);
@@ -392,8 +393,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!mbar_wait_warp(&q_full[s], ph, ctl)) break;  // LSE and D of this tile are in smem
       if (!mbar_wait_warp(s_full, it & 1, ctl)) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512) + 64 * half;
-      const float* dl = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + 64 * half;
+      const float* nl2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512) + 64 * half;
+      const float* nd = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + 64 * half;
+      const float2 cc = make_float2(c2, c2);
       const bool diag = a.causal && (i == j);
       uint32_t p[32];
 #pragma unroll
@@ -405,12 +407,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int ql = 32 * c + 4 * e;  // query within this half
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + ql);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          float x[4];
+          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + ql);  // -LSE * log2(e)
+          const float2 y0 = fma2(make_float2(__uint_as_float(sv[4 * e]), __uint_as_float(sv[4 * e + 1])),
+                                 cc, make_float2(l4.x, l4.y));
+          const float2 y1 = fma2(make_float2(__uint_as_float(sv[4 * e + 2]), __uint_as_float(sv[4 * e + 3])),
+                                 cc, make_float2(l4.z, l4.w));
+          float x[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            x[u] = ex2(fmaf(__uint_as_float(sv[4 * e + u]), c2, -lv[u]));
             if (diag) x[u] = (r <= 64 * half + ql + u) ? x[u] : 0.f;  // key > query: masked
             if (!row_live) x[u] = 0.f;
           }
@@ -436,12 +440,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int ql = 32 * c + 4 * e;
-          const float4 d4 = *reinterpret_cast<const float4*>(dl + ql);
+          const float4 d4 = *reinterpret_cast<const float4*>(nd + ql);  // -D
           const uint32_t pa = p[16 * c + 2 * e], pb = p[16 * c + 2 * e + 1];
-          ds[2 * e] = pack_bf16(bf16_lo(pa) * (__uint_as_float(dv[4 * e]) - d4.x),
-                                bf16_hi(pa) * (__uint_as_float(dv[4 * e + 1]) - d4.y));
-          ds[2 * e + 1] = pack_bf16(bf16_lo(pb) * (__uint_as_float(dv[4 * e + 2]) - d4.z),
-                                    bf16_hi(pb) * (__uint_as_float(dv[4 * e + 3]) - d4.w));
+          const float2 t0 = add2(make_float2(__uint_as_float(dv[4 * e]), __uint_as_float(dv[4 * e + 1])),
+                                 make_float2(d4.x, d4.y));
+          const float2 t1 = add2(make_float2(__uint_as_float(dv[4 * e + 2]), __uint_as_float(dv[4 * e + 3])),
+                                 make_float2(d4.z, d4.w));
+          const float2 u0 = mul2(make_float2(bf16_lo(pa), bf16_hi(pa)), t0);
+          const float2 u1 = mul2(make_float2(bf16_lo(pb), bf16_hi(pb)), t1);
+          ds[2 * e] = pack_bf16(u0.x, u0.y);
+          ds[2 * e + 1] = pack_bf16(u1.x, u1.y);
         }
         // dS^T packed over dP^T columns this half has already read (A operand of dK += dS^T Q)
         tmem_st16(tDP + 16 * c, ds);
@@ -550,15 +558,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse, int BH,
-                                  int N, float* lse2, float* delta, float* dq_acc, cudaStream_t s) {
+                                  int N, float* neg_lse2, float* neg_delta, float* dq_acc,
+                                  cudaStream_t s) {
   const int nqt = (N + 127) / 128;
   const dim3 grid(nqt, BH);
   auto o = static_cast<const __nv_bfloat16*>(O);
   auto g = static_cast<const __nv_bfloat16*>(dO);
   if (d == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, lse2, delta, dq_acc);
+    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc);
   else
-    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, lse2, delta, dq_acc);
+    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc);
   return cudaGetLastError();
 }
 

@@ -30,17 +30,17 @@ struct BwdArgs {
   float scale;            // softmax scale (dK is scaled by it at the end)
   float scale_log2;       // scale * log2(e)
   const int32_t* kv_lens;
-  const float* lse2;      // workspace: LSE * log2(e), [BH][Npad], +inf on padded rows
-  const float* delta;     // workspace: D = rowsum(dO o O), [BH][Npad], 0 on padded rows
+  const float* neg_lse2;  // workspace: -LSE * log2(e), [BH][Npad], -inf on padded rows
+  const float* neg_delta; // workspace: -D = -rowsum(dO o O), [BH][Npad], 0 on padded rows
   float* dq_acc;          // workspace: dQ accumulator, tile-major (see fa_bwd.cu)
   int* status;
   uint64_t timeout_ns;
   uint32_t smem_bytes;
 };
 
-// Workspace layout (all offsets 256-byte aligned): dq_acc | lse2 | delta
+// Workspace layout (all offsets 256-byte aligned): dq_acc | -LSE*log2(e) | -D
 struct Workspace {
-  size_t dq_acc_off, lse2_off, delta_off, total;
+  size_t dq_acc_off, neg_lse2_off, neg_delta_off, total;
 };
 Workspace workspace_layout(int BH, int N, int d);
 
@@ -48,7 +48,7 @@ Workspace workspace_layout(int BH, int N, int d);
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse,
-                                  int BH, int N, float* lse2, float* delta, float* dq_acc,
+                                  int BH, int N, float* neg_lse2, float* neg_delta, float* dq_acc,
                                   cudaStream_t s);
 cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
