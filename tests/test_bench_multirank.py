@@ -1,0 +1,45 @@
+"""bench.py's multi-process path on the CPU: two gloo ranks launched by torchrun run the
+reference (oracle) arm; rank 0 alone prints one JSON line and every rank exits 0."""
+
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_two_ranks_gloo():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="2")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", "--master-port=29533", os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0",
+           "--workload", "smoke-1x1x128x64"]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_max_over_ranks_gloo(tmp_path):
+    """The timing reduction used by bench.py: the max of the ranks' times."""
+    script = tmp_path / "ranks.py"
+    script.write_text(
+        "import sys, torch.distributed as dist\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "dist.init_process_group('gloo')\n"
+        "r = dist.get_rank()\n"
+        "m = bench.max_over_ranks(1.0 + r, 2)\n"
+        "assert m == 2.0, m\n"
+        "bench.barrier(2)\n"
+        "dist.destroy_process_group()\n")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", "--master-port=29534", str(script)]
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
