@@ -34,8 +34,10 @@ from exact_io_aware_fwd_gb300.workloads import BY_NAME, HEADLINE, workload_input
 
 METRIC = "attention fwd/bwd TFLOPS (bf16, 1\u00d7GB300) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-SOURCES_FOR_TRAFFIC = ["exact_io_aware_fwd_gb300/csrc/fa_bwd.cu",
+SOURCES_FOR_TRAFFIC = ["exact_io_aware_fwd_gb300/csrc/fa_api.cu",
+                       "exact_io_aware_fwd_gb300/csrc/fa_bwd.cu",
                        "exact_io_aware_fwd_gb300/csrc/fa_fwd.cu",
+                       "exact_io_aware_fwd_gb300/csrc/fa_internal.h",
                        "exact_io_aware_fwd_gb300/csrc/sm103.cuh"]
 
 

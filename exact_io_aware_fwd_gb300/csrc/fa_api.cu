@@ -142,6 +142,12 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   a.N = N;
   a.BH = BH;
   a.num_qblocks = (N + 255) / 256;
+  {
+    // heads whose K and V (2 * N * d bf16 each) fit in 64 MB, about half of the 129 MB L2
+    const long long kv_bytes = 4LL * N * d;
+    const long long g = (64LL << 20) / (kv_bytes > 0 ? kv_bytes : 1);
+    a.head_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  }
   a.causal = causal ? 1 : 0;
   a.scale_log2 = resolve_scale(scale, d) * kLog2e;
   a.kv_lens = kv_lens;

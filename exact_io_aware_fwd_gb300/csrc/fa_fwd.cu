@@ -111,13 +111,17 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
 
-  // ---- work item: block level major, all heads of one level together; causal: the heaviest
-  // blocks first, so that every wave holds CTAs of similar length and the light ones fill the
-  // tail (measured on GB300: 6% faster than head-major on the long causal case; within 2% either
-  // way on the non-causal cases)
+  // ---- work item: heads in groups of `head_group` whose K/V fit in about half of L2; within a
+  // group block level major (all heads of one level together) and, with a causal mask, the
+  // heaviest blocks first, so that every wave holds CTAs of similar length and the light ones
+  // fill the tail.  Groups run one after another.
   const int lin = blockIdx.x;
-  const int bh = lin % a.BH;
-  const int qb = a.causal ? (a.num_qblocks - 1 - lin / a.BH) : (lin / a.BH);
+  const int gsz = a.head_group * a.num_qblocks;  // CTAs per full group
+  const int grp = lin / gsz;
+  const int heads = min(a.head_group, a.BH - grp * a.head_group);  // heads in this group
+  const int idx = lin - grp * gsz;
+  const int bh = grp * a.head_group + idx % heads;
+  const int qb = a.causal ? (a.num_qblocks - 1 - idx / heads) : (idx / heads);
   const int b = bh / a.H;
   const int N = a.N;
   int kv_len = N;

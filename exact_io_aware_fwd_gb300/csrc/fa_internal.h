@@ -14,6 +14,7 @@ constexpr int kTileRows = 128;  // query rows per Q tile and keys per K/V tile
 struct FwdArgs {
   int H, N, BH;
   int num_qblocks;        // 256-row query blocks per (b, h)
+  int head_group;         // heads scheduled together (their K/V stay resident in L2)
   int causal;
   float scale_log2;       // scale * log2(e)
   const int32_t* kv_lens; // device int32[B] or nullptr
