@@ -63,7 +63,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * Bytes of workspace fa_bwd needs for these sizes: a float32 dQ accumulator plus the per-row
- * statistics D = rowsum(dO o O) and LSE * log2(e), each padded to a multiple of 128 rows per
+ * statistics -D = -rowsum(dO o O) and -LSE * log2(e), each padded to a multiple of 128 rows per
  * (b, h).  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
@@ -85,7 +85,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 /*
  * The three stages of fa_bwd, exported so that each can be launched (and timed) on its own.
  * They must run in this order on one stream with the same arguments and workspace.
- *  fa_bwd_preprocess: D_i = sum_k dO_ik O_ik, LSE_i * log2(e) into the workspace, and zeroes
+ *  fa_bwd_preprocess: -D_i = -sum_k dO_ik O_ik, -LSE_i * log2(e) into the workspace, zeroes
  *                     the dQ accumulator (first page, 关键设计三, D_i = dO_i^T O_i).
  *  fa_bwd_dkdv:       one pass over the query tiles per key tile: recomputes P^T from LSE,
  *                     writes dK, dV and adds dS K into the dQ accumulator with float32
