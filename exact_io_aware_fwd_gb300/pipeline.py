@@ -15,11 +15,21 @@ import torch
 from . import binding
 
 
-def _chunks(B, H, heads_per_chunk):
-    """(b, h0, h1) ranges of whole heads; each is a contiguous slice of a [B, H, N, d] tensor."""
+def _chunks(B, H, target=8, heads_per_chunk=None):
+    """(b0, b1, h0, h1) pieces, each a contiguous slice q[b0:b1, h0:h1] of a [B, H, N, d] tensor:
+    about `target` pieces of whole batches when B >= target, otherwise head ranges of one batch
+    (`heads_per_chunk` overrides the head-range width)."""
+    if heads_per_chunk is None and B >= target:
+        per = -(-B // target)
+        for b0 in range(0, B, per):
+            yield b0, min(B, b0 + per), 0, H
+        return
+    if heads_per_chunk is None:
+        heads_per_chunk = max(1, -(-(B * H) // target))
+    heads_per_chunk = min(heads_per_chunk, H)
     for b in range(B):
         for h0 in range(0, H, heads_per_chunk):
-            yield b, h0, min(H, h0 + heads_per_chunk)
+            yield b, b + 1, h0, min(H, h0 + heads_per_chunk)
 
 
 class HostAttention:
@@ -34,11 +44,8 @@ class HostAttention:
         self.o, self.dq, self.dk, self.dv = mk(), mk(), mk(), mk()
         self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         self.kv = torch.empty((B,), dtype=torch.int32, device=dev)
-        if heads_per_chunk is None:  # about 8 chunks in flight
-            heads_per_chunk = max(1, (B * H) // 8) if B == 1 else H
-            heads_per_chunk = min(heads_per_chunk, H)
-        self.plan = list(_chunks(B, H, heads_per_chunk))
-        max_heads = max(h1 - h0 for _, h0, h1 in self.plan)
+        self.plan = list(_chunks(B, H, heads_per_chunk=heads_per_chunk))
+        max_heads = max((b1 - b0) * (h1 - h0) for b0, b1, h0, h1 in self.plan)
         # chunks compute one after another on one stream, so one workspace serves them all
         self.workspace = torch.empty(binding.fa_bwd_workspace_size(1, max_heads, N, d),
                                      dtype=torch.uint8, device=dev)
@@ -60,8 +67,8 @@ class HostAttention:
         if kv_lens is not None:
             with torch.cuda.stream(self.s_in):
                 self.kv.copy_(kv_lens.to(torch.int32), non_blocking=True)
-        for b, h0, h1 in self.plan:
-            sl = (b, slice(h0, h1))
+        for b0, b1, h0, h1 in self.plan:
+            sl = (slice(b0, b1), slice(h0, h1))
             with torch.cuda.stream(self.s_in):
                 for dst, src in ((self.q, q), (self.k, k), (self.v, v), (self.do, do)):
                     dst[sl].copy_(src[sl], non_blocking=True)
@@ -69,9 +76,9 @@ class HostAttention:
                 ev_in.record(self.s_in)
             self.s_comp.wait_event(ev_in)
             with torch.cuda.stream(self.s_comp):
-                view = lambda t: t[sl].unsqueeze(0)  # noqa: E731  [1, h1-h0, N, d], contiguous
-                kv = self.kv[b:b + 1] if kv_lens is not None else None
-                o, lse = view(self.o), self.lse[sl].unsqueeze(0)
+                view = lambda t: t[sl]  # noqa: E731  [b1-b0, h1-h0, N, d], contiguous
+                kv = self.kv[b0:b1] if kv_lens is not None else None
+                o, lse = view(self.o), self.lse[sl]
                 binding.fa_fwd(view(self.q), view(self.k), view(self.v), causal=causal,
                                scale=scale, kv_lens=kv, out=o, lse=lse, stream=self.s_comp)
                 binding.fa_bwd(view(self.q), view(self.k), view(self.v), o, view(self.do), lse,
