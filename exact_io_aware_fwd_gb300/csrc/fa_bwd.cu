@@ -13,11 +13,11 @@
 //                  -inf, which makes their recomputed P exactly 0), and zeroes the float32 dQ
 //                  accumulator.
 //  bwd_dkdv        one CTA per (b, h, 128-key tile j); dK_j and dV_j accumulate in tensor memory
-//                  over the query tiles i (causal: i >= j only).  16 warps: TMA producer, MMA
-//                  issuer, two warpgroups that each handle 64 of the 128 query columns of every
-//                  key row for P and dS (two warps per SM sub-partition hide each other's
-//                  tensor-memory and shared-memory latency), and a warpgroup that drains dQ_i
-//                  and writes dK, dV at the end.  Per query tile:
+//                  over the query tiles i (causal: i >= j only).  Warps: TMA producer, MMA
+//                  issuer, two idle, and kGroups warpgroups that each handle 128 / kGroups of
+//                  the 128 query columns of every key row for P and dS, drain their share of
+//                  dQ_{i-1} between P_i and dS_i (while dP_i runs), and write their share of the
+//                  dV and dK panels at the end.  Per query tile:
 //                    S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (tcgen05, both operands in smem)
 //                    P^T = exp2(S^T * scale * log2 e - LSE_i * log2 e), written back over S^T
 //                    dS^T = P^T o (dP^T - D_i), written back over dP^T and to smem
@@ -162,10 +162,24 @@ struct BwdLayout {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// Packed bf16 column of the 16-query k-step kk (0..7) inside the S^T or dP^T region.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+// Warpgroups sharing the elementwise work (P, dS, the dQ drain, the epilogue); each owns
+// 128 / kGroups query columns of every key row.  Measured on GB300: 4 groups are no faster
+// than 2 at d = 128 and 6% slower at d = 64 (the kernel is bound by moving the fp32 dQ
+// partials to L2 and by shared-memory traffic, not by the latency of these phases).
+#ifndef FA_BWD_GROUPS
+#define FA_BWD_GROUPS 2
+#endif
+constexpr int kGroups = FA_BWD_GROUPS;
+constexpr int kQG = 128 / kGroups;  // query columns per group
+static_assert(kGroups == 2 || kGroups == 4, "two or four elementwise warpgroups");
 
-constexpr int kBwdThreads = 512;
+// Packed bf16 column of the 16-query k-step kk (0..7) inside the S^T or dP^T region: a group
+// writes its packed values over the first half of its own columns.
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return (16 * kk / kQG) * kQG + ((16 * kk) % kQG) / 2;
+}
+
+constexpr int kBwdThreads = 128 * (1 + kGroups);
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -220,11 +234,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
     for (int k = 0; k < L::kNumBars; ++k) {
-      // P and dS are signalled by the eight warps of the two P/dS warpgroups, the dQ release by
-      // the four drain warps
+      // P, dS and the release of dQ_i's tensor memory are signalled by every warp of the
+      // elementwise warpgroups
       uint32_t count = 1;
-      if (&bars[k] == p_full || &bars[k] == ds_full) count = 8;
-      if (&bars[k] == dq_empty) count = 4;
+      if (&bars[k] == p_full || &bars[k] == ds_full || &bars[k] == dq_empty) count = 4 * kGroups;
       mbar_init(&bars[k], count);
     }
     fence_mbar_init();
@@ -290,45 +303,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // tile i: dK(i), dQ(i) | dV(i+1), dP(i+1) | S(i+2).  The tensor pipe always has the next
       // tile's work queued while the P/dS warpgroups compute, and dV(i+1) covers the drain of
       // dQ(i) that dP(i+1) waits for.  Q_i is released after dK(i), dO_i after dV(i).
+      // descriptors of each operand buffer; a k-step adds its byte offset to the start address
+      const uint64_t desc_k = sdesc_sw128(kb, 16384, 1024), desc_v = sdesc_sw128(vb, 16384, 1024);
+      const uint64_t desc_ds = sdesc_sw128(dsb, 16384, 1024);
+      auto desc_q = [&](int it) {
+        return sdesc_sw128(sbase + L::kQ + (it & 1) * L::kTile, 16384, 1024);
+      };
+      auto desc_do = [&](int it) {
+        return sdesc_sw128(sbase + L::kDO + (it & 1) * L::kTile, 16384, 1024);
+      };
+      auto kmaj = [](int kk) -> uint64_t {  // K-major k-step: 32 B inside a panel, 16 KB panels
+        return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+      };
       auto issue_S = [&](int it) {  // S^T = K_j Q_i^T
-        const uint32_t qb = sbase + L::kQ + (it & 1) * L::kTile;
+        const uint64_t dq = desc_q(it);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + L::kColS, sdesc_sw128(kb + off, 16384, 1024),
-                 sdesc_sw128(qb + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + L::kColS, desc_k + kmaj(kk), dq + kmaj(kk), idS, kk > 0 ? 1u : 0u);
         mma_commit(s_full);
       };
       auto issue_dP = [&](int it) {  // dP^T = V_j dO_i^T
-        const uint32_t dob = sbase + L::kDO + (it & 1) * L::kTile;
+        const uint64_t ddo = desc_do(it);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tmem + L::kColDP, sdesc_sw128(vb + off, 16384, 1024),
-                 sdesc_sw128(dob + off, 16384, 1024), idS, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + L::kColDP, desc_v + kmaj(kk), ddo + kmaj(kk), idS, kk > 0 ? 1u : 0u);
         mma_commit(dp_full);
       };
-      auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA)
-        const uint32_t dob = sbase + L::kDO + (it & 1) * L::kTile;
+      auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA: +2 KB rows)
+        const uint64_t ddo = desc_do(it);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + L::kColDV, tmem + L::kColS + packed_col(kk),
-                 sdesc_sw128(dob + kk * 2048, 16384, 1024), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kColDV, tmem + L::kColS + packed_col(kk), ddo + kk * 128, idKV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&do_empty[it & 1]);
       };
       auto issue_dK_dQ = [&](int it) {
-        const uint32_t qb = sbase + L::kQ + (it & 1) * L::kTile;
+        const uint64_t dq = desc_q(it);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + L::kColDK, tmem + L::kColDP + packed_col(kk),
-                 sdesc_sw128(qb + kk * 2048, 16384, 1024), idKV, (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + L::kColDK, tmem + L::kColDP + packed_col(kk), dq + kk * 128, idKV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&q_empty[it & 1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
-          mma_ss(tmem + L::kColDP, sdesc_sw128(dsb + kk * 2048, 16384, 1024),
-                 sdesc_sw128(kb + kk * 2048, 16384, 1024), idQ, kk > 0 ? 1u : 0u);
+          mma_ss(tmem + L::kColDP, desc_ds + kk * 128, desc_k + kk * 128, idQ, kk > 0 ? 1u : 0u);
         mma_commit(dq_full);
       };
       auto wait_q = [&](int it) { return mbar_wait(&q_full[it & 1], (it >> 1) & 1, ctl); };
@@ -375,38 +393,75 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(mma_done);
       drain_wait(mma_done, 0, ctl);
     }
-  } else if (warp >= 4 && warp < 12) {
-    // ================= P and dS: one thread per key row, one warpgroup per 64-query half
+  } else if (warp >= 4) {
+    // ================= P, dS, the dQ drain and the epilogue: one thread per row of the tile,
+    // one warpgroup per kQG query columns of P / dS and D / kGroups columns of dQ
     const uint32_t quad = warp & 3;
-    const int half = (warp - 4) >> 2;
+    const int grp = (warp - 4) >> 2;
+    const int q0 = kQG * grp;  // first query column of this group
     const int r = quad * 32 + lane;
     const int key = j * 128 + r;
     const bool row_live = key < kv_len;
     const uint32_t lanes = (quad * 32u) << 16;
-    const uint32_t tS = tmem + lanes + L::kColS + 64 * half;
-    const uint32_t tDP = tmem + lanes + L::kColDP + 64 * half;
+    const uint32_t tS = tmem + lanes + L::kColS + q0;
+    const uint32_t tDP = tmem + lanes + L::kColDP + q0;
+    constexpr int kDC = D / kGroups;  // dQ columns drained by this group
+    const uint32_t tDQ = tmem + lanes + L::kColDP + kDC * grp;
     const float c2 = a.scale_log2;
-    const uint32_t dsb = sbase + L::kDS + half * 16384;
+
+    // dQ_i (query row r of the tile, this group's columns) into the fp32 accumulator: load,
+    // release the tensor memory (dP_{i+1} waits for it), then the atomics, which overlap dP_{i+1}
+    auto drain = [&](int it) -> bool {
+      if (!mbar_wait_warp(dq_full, it & 1, ctl)) return false;
+      tc_fence_after();
+      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + i0 + it) * 128 * D;
+      const int g0 = (kDC / 4) * grp;  // first 4-column group of this group's columns
+      uint32_t va[32], vb[32];
+      if (kDC >= 32) tmem_ld32(tDQ, va);
+      if (kDC == 64) tmem_ld32(tDQ + 32, vb);
+      if (kDC == 16) tmem_ld16(tDQ, *reinterpret_cast<uint32_t(*)[16]>(&va[0]));
+      tmem_wait_ld();
+      reg_fence(va);
+      if (kDC == 64) reg_fence(vb);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+#pragma unroll
+      for (int g = 0; g < (kDC >= 32 ? 8 : 4); ++g)
+        red_add_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(va[4 * g]),
+                   __uint_as_float(va[4 * g + 1]), __uint_as_float(va[4 * g + 2]),
+                   __uint_as_float(va[4 * g + 3]));
+      if (kDC == 64) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g)
+          red_add_v4(tile + ((g0 + 8 + g) * 128 + r) * 4, __uint_as_float(vb[4 * g]),
+                     __uint_as_float(vb[4 * g + 1]), __uint_as_float(vb[4 * g + 2]),
+                     __uint_as_float(vb[4 * g + 3]));
+      }
+      return true;
+    };
+
+    bool ok = true;
     for (int it = 0; it < nI; ++it) {
       const int i = i0 + it, s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (!mbar_wait_warp(&q_full[s], ph, ctl)) break;  // LSE and D of this tile are in smem
-      if (!mbar_wait_warp(s_full, it & 1, ctl)) break;
+      if (!(ok = mbar_wait_warp(&q_full[s], ph, ctl))) break;  // LSE and D are in smem
+      if (!(ok = mbar_wait_warp(s_full, it & 1, ctl))) break;
       tc_fence_after();
-      const float* nl2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512) + 64 * half;
-      const float* nd = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + 64 * half;
+      const float* nl2 = reinterpret_cast<const float*>(sm + L::kLse + s * 512) + q0;
+      const float* nd = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + q0;
       const float2 cc = make_float2(c2, c2);
       const bool diag = a.causal && (i == j);
-      uint32_t p[32];
+      uint32_t p[kQG / 2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kQG / 32; ++c) {
         uint32_t sv[32];
         tmem_ld32(tS + 32 * c, sv);
         tmem_wait_ld();
         reg_fence(sv);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int ql = 32 * c + 4 * e;  // query within this half
+          const int ql = 32 * c + 4 * e;  // query within this group
           const float4 l4 = *reinterpret_cast<const float4*>(nl2 + ql);  // -LSE * log2(e)
           const float2 y0 = fma2(make_float2(__uint_as_float(sv[4 * e]), __uint_as_float(sv[4 * e + 1])),
                                  cc, make_float2(l4.x, l4.y));
@@ -415,23 +470,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float x[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            if (diag) x[u] = (r <= 64 * half + ql + u) ? x[u] : 0.f;  // key > query: masked
+            if (diag) x[u] = (r <= q0 + ql + u) ? x[u] : 0.f;  // key > query: masked
             if (!row_live) x[u] = 0.f;
           }
           p[16 * c + 2 * e] = pack_bf16(x[0], x[1]);
           p[16 * c + 2 * e + 1] = pack_bf16(x[2], x[3]);
         }
       }
-      tmem_st32(tS, p);  // P^T over this half's first 32 columns (all of its S^T was read)
+      // P^T over the first half of this group's columns (all of its S^T was read)
+      if (kQG == 64) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+      else tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&p[0]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
 
-      if (!mbar_wait_warp(dp_full, it & 1, ctl)) break;
+      if (it > 0 && !(ok = drain(it - 1))) break;
+
+      if (!(ok = mbar_wait_warp(dp_full, it & 1, ctl))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < kQG / 32; ++c) {
         uint32_t dv[32];
         tmem_ld32(tDP + 32 * c, dv);
         tmem_wait_ld();
@@ -451,13 +510,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ds[2 * e] = pack_bf16(u0.x, u0.y);
           ds[2 * e + 1] = pack_bf16(u1.x, u1.y);
         }
-        // dS^T packed over dP^T columns this half has already read (A operand of dK += dS^T Q)
+        // dS^T packed over dP^T columns this group has already read (A operand of dK += dS^T Q)
         tmem_st16(tDP + 16 * c, ds);
         // and to smem as [key row][query], 128-byte swizzled (A operand of dQ = dS K)
+        const int qa = q0 + 32 * c;  // absolute first query of this chunk
+        const uint32_t panel = sbase + L::kDS + (qa >> 6) * 16384;
 #pragma unroll
         for (int g = 0; g < 4; ++g)
-          st_shared_v4(dsb + sw128_offset(r, 4 * c + g), ds[4 * g], ds[4 * g + 1], ds[4 * g + 2],
-                       ds[4 * g + 3]);
+          st_shared_v4(panel + sw128_offset(r, ((qa & 63) >> 3) + g), ds[4 * g], ds[4 * g + 1],
+                       ds[4 * g + 2], ds[4 * g + 3]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -465,54 +526,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-  } else if (warp >= 12) {
-    // ================= dQ reduction and the dK / dV epilogue: one thread per row
-    const uint32_t quad = warp & 3;
-    const int r = quad * 32 + lane;
-    const uint32_t lanes = (quad * 32u) << 16;
-    const uint32_t tDP = tmem + lanes + L::kColDP;
-    bool ok = true;
-    for (int it = 0; it < nI; ++it) {
-      const int i = i0 + it;
-      if (!(ok = mbar_wait_warp(dq_full, it & 1, ctl))) break;
-      tc_fence_after();
-      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {  // 64 columns per round: two loads, then the atomics
-        uint32_t va[32], vb[32];
-        tmem_ld32(tDP + 64 * c, va);
-        tmem_ld32(tDP + 64 * c + 32, vb);
-        tmem_wait_ld();
-        reg_fence(va);
-        reg_fence(vb);
-        if (c == D / 64 - 1) {  // tensor memory fully read: release it before the reductions
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(dq_empty);
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          red_add_v4(tile + ((16 * c + g) * 128 + r) * 4, __uint_as_float(va[4 * g]),
-                     __uint_as_float(va[4 * g + 1]), __uint_as_float(va[4 * g + 2]),
-                     __uint_as_float(va[4 * g + 3]));
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          red_add_v4(tile + ((16 * c + 8 + g) * 128 + r) * 4, __uint_as_float(vb[4 * g]),
-                     __uint_as_float(vb[4 * g + 1]), __uint_as_float(vb[4 * g + 2]),
-                     __uint_as_float(vb[4 * g + 3]));
-      }
-    }
+    if (ok && nI > 0) ok = drain(nI - 1);
+
+    // ---- epilogue: the 64-column panels of dV and scale * dK (bf16, swizzled, over the V or K
+    // tile in smem, which no MMA reads any more) are shared out over the groups; one TMA store
+    // per panel
     if (ok && nI > 0) ok = mbar_wait_warp(dkdv_full, 0, ctl);
-    if (ok) {
-      if (nI > 0) tc_fence_after();
-      // dV -> V tile buffer, scale * dK -> K tile buffer (bf16, swizzled), then TMA stores
+    constexpr int kPanels = 2 * (D / 64);  // dV panels, then dK panels
+    if (ok && nI > 0) tc_fence_after();
+    for (int pn = grp; pn < kPanels; pn += kGroups) {
+      const bool is_dk = pn >= D / 64;
+      const int cp = pn % (D / 64);  // column panel within the matrix
+      const uint32_t col = (is_dk ? L::kColDK : L::kColDV) + 64 * cp;
+      const float mul = is_dk ? a.scale : 1.f;
+      const uint32_t panel = sbase + (is_dk ? L::kK : L::kV) + cp * 16384;
+      if (ok) {
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
-        const float mul = which == 0 ? 1.f : a.scale;
-        const uint32_t buf = sbase + (which == 0 ? L::kV : L::kK);
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
           if (nI > 0) {
             tmem_ld32(tmem + lanes + col + 32 * c, v);
@@ -526,24 +556,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
-          const uint32_t panel = buf + ((32 * c) / 64) * 16384;
-          const uint32_t g0 = ((32 * c) % 64) / 8;
 #pragma unroll
           for (int g = 0; g < 4; ++g)
-            st_shared_v4(panel + sw128_offset(r, g0 + g), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2],
-                         pk[4 * g + 3]);
+            st_shared_v4(panel + sw128_offset(r, 4 * c + g), pk[4 * g], pk[4 * g + 1],
+                         pk[4 * g + 2], pk[4 * g + 3]);
         }
       }
-    }
-    fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (quad == 0 && lane == 0 && !*abort_flag) {
-      for (int c = 0; c < D / 64; ++c) {
-        tma_store_3d(&tmdV, sm + L::kV + c * 16384, c * 64, j * 128, bh);
-        tma_store_3d(&tmdK, sm + L::kK + c * 16384, c * 64, j * 128, bh);
+      fence_proxy_async_smem();
+      named_bar_sync(1 + grp, 128);  // every warp of the group arrives, aborted or not
+      if (quad == 0 && lane == 0 && !*abort_flag) {
+        tma_store_3d(is_dk ? &tmdK : &tmdV, sm + (is_dk ? L::kK : L::kV) + cp * 16384, cp * 64,
+                     j * 128, bh);
+        bulk_commit();
+        bulk_wait_read0();
       }
-      bulk_commit();
-      bulk_wait_read0();
     }
   }
 
