@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=HEADLINE.name, choices=sorted(BY_NAME))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--bwd", default="atomic", choices=["atomic", "deterministic"],
+                    help="backward entry: fa_bwd (dQ by fp32 atomics) or fa_bwd_deterministic")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=None,
@@ -258,9 +260,23 @@ def run_ours(args, w, world, rank, local):
     ws = fa.workspace_for(qd)
     f_fwd, f_bwd = w.flops()
 
-    stages = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    det = args.bwd == "deterministic"
+    stages = ["fwd", "bwd"] if det else ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+
+    def step_det(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
+        if evs is not None:
+            evs[1].record(stream)
+        fa.fa_bwd_deterministic(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale,
+                                kv_lens=kvd, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if evs is not None:
+            evs[2].record(stream)
 
     def step(evs=None):
+        if det:
+            return step_det(evs)
         if evs is not None:
             evs[0].record(stream)
         fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
@@ -322,7 +338,8 @@ def run_ours(args, w, world, rank, local):
         h2d, d2h = ha.transfer_bytes(with_kv=kv is not None)
 
         def e2e_step():
-            ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout)
+            ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout,
+                   deterministic=det)
 
         for _ in range(2):
             e2e_step()
@@ -346,11 +363,13 @@ def run_ours(args, w, world, rank, local):
 
     # ---- roofline of the dominant kernel (largest share of the step)
     peaks, src = load_peaks()
-    dom = max(("fwd", "bwd_dkdv"), key=lambda s: stage_ms[s])
+    bwd_stage = "bwd" if det else "bwd_dkdv"
+    dom = max(("fwd", bwd_stage), key=lambda s: stage_ms[s])
     dom_flops = f_fwd if dom == "fwd" else f_bwd
     achieved = dom_flops / (stage_ms[dom] * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel"}[dom]
+    kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel",
+                   "bwd": "bwd_dkdv_kernel+bwd_dq_kernel"}[dom]
     roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"bf16_tflops (burst) of {src}",
@@ -363,7 +382,7 @@ def run_ours(args, w, world, rank, local):
                "kind": "oracle", "sample": sample, "seconds": dt}
 
     fwd_tf = f_fwd / (stage_ms["fwd"] * 1e-3) / 1e12
-    bwd_ms = stage_ms["bwd_preprocess"] + stage_ms["bwd_dkdv"] + stage_ms["bwd_dq_convert"]
+    bwd_ms = sum(stage_ms[s] for s in stages[1:])
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -373,7 +392,7 @@ def run_ours(args, w, world, rank, local):
                    "kv_lens": None if kv is None else kv.tolist(),
                    "l2": "inputs larger than L2 (no flush)" if 4 * q.numel() * 2 > 129e6 else
                    "inputs smaller than L2 (not flushed)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "bwd": args.bwd},
         "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,

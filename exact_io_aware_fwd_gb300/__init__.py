@@ -16,6 +16,7 @@ from .binding import (  # noqa: F401
     FAError,
     default_scale,
     fa_bwd,
+    fa_bwd_deterministic,
     fa_bwd_dkdv,
     fa_bwd_dq_convert,
     fa_bwd_noalloc,

@@ -31,6 +31,7 @@ EXPORTED = [
     "fa_bwd_dkdv",
     "fa_bwd_dq_convert",
     "fa_bwd_noalloc",
+    "fa_bwd_deterministic",
     "fa_get_error",
     "fa_status_string",
 ]
@@ -68,6 +69,9 @@ def load_library(path: str | None = None):
     lib.fa_bwd_dq_convert.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp]
     lib.fa_bwd_noalloc.restype = i
+    lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                          vp, vp, sz, vp]
+    lib.fa_bwd_deterministic.restype = i
     lib.fa_get_error.argtypes = [vp]
     lib.fa_get_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -159,6 +163,23 @@ def fa_bwd(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dq=None,
                                _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), _scale(scale),
                                _ptr(kv), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_deterministic(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dq=None,
+                         dk=None, dv=None, workspace=None, stream=None):
+    """fa_bwd with run-to-run bit-identical results (dQ without atomics; see include/fa.h)."""
+    B, H, N, d = _check_qkv(q, k, v, o, do)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace_for(q) if workspace is None else workspace
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
+                                             _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                             int(bool(causal)), _scale(scale), _ptr(kv), _ptr(ws),
+                                             ws.numel(), _stream(stream))
+    _check(st, "fa_bwd_deterministic")
     return dq, dk, dv
 
 

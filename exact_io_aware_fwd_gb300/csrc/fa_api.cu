@@ -173,34 +173,43 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE, int
   cudaError_t e = fa::launch_bwd_preprocess(
       d, O, dO, LSE, BH, N, reinterpret_cast<float*>(ws + w.neg_lse2_off),
       reinterpret_cast<float*>(ws + w.neg_delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
-      static_cast<cudaStream_t>(stream));
+      /*zero_acc=*/true, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK,
-                      void* dV, int B, int H, int N, int d, int causal, float scale,
-                      const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
-                      void* stream) {
-  fa_status st = check_sizes(B, H, N, d);
-  if (st != FA_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// Validation, tensor maps and arguments shared by the dK/dV and the deterministic dQ kernels.
+struct BwdSetup {
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv, tdq;
+  fa::BwdArgs a{};
+};
+
+fa_status bwd_setup(BwdSetup& st, const void* Q, const void* K, const void* V, const void* dO,
+                    void* dK, void* dV, void* dQ, int B, int H, int N, int d, int causal,
+                    float scale, const int32_t* kv_lens, void* workspace, size_t workspace_bytes) {
+  fa_status rc = check_sizes(B, H, N, d);
+  if (rc != FA_OK) return rc;
   if (!Q || !K || !V || !dO || !dK || !dV) return FA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dK) ||
-      !aligned16(dV))
+      !aligned16(dV) || (dQ && !aligned16(dQ)))
     return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   const int BH = B * H;
-  if ((st = check_workspace(workspace, workspace_bytes, BH, N, d)) != FA_OK) return st;
-  if ((st = check_device()) != FA_OK) return st;
+  if ((rc = check_workspace(workspace, workspace_bytes, BH, N, d)) != FA_OK) return rc;
+  if ((rc = check_device()) != FA_OK) return rc;
   int* status = status_ptr();
   if (status == nullptr) return FA_ERR_CUDA;
-  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  if (!make_tile_map(&tq, Q, BH, N, d) || !make_tile_map(&tk, K, BH, N, d) ||
-      !make_tile_map(&tv, V, BH, N, d) || !make_tile_map(&tdo, dO, BH, N, d) ||
-      !make_tile_map(&tdk, dK, BH, N, d) || !make_tile_map(&tdv, dV, BH, N, d))
+  if (!make_tile_map(&st.tq, Q, BH, N, d) || !make_tile_map(&st.tk, K, BH, N, d) ||
+      !make_tile_map(&st.tv, V, BH, N, d) || !make_tile_map(&st.tdo, dO, BH, N, d) ||
+      !make_tile_map(&st.tdk, dK, BH, N, d) || !make_tile_map(&st.tdv, dV, BH, N, d) ||
+      (dQ && !make_tile_map(&st.tdq, dQ, BH, N, d)))
     return FA_ERR_CUDA;
   const fa::Workspace w = fa::workspace_layout(BH, N, d);
   char* ws = static_cast<char*>(workspace);
-  fa::BwdArgs a{};
+  fa::BwdArgs& a = st.a;
   a.H = H;
   a.N = N;
   a.BH = BH;
@@ -215,8 +224,49 @@ fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* d
   a.status = status;
   a.timeout_ns = wait_timeout_ns();
   if (static_cast<long long>(a.num_qtiles) * BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  cudaError_t e =
-      fa::launch_bwd_dkdv(d, tq, tk, tv, tdo, tdk, tdv, a, static_cast<cudaStream_t>(stream));
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* dO, void* dK,
+                      void* dV, int B, int H, int N, int d, int causal, float scale,
+                      const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  BwdSetup st;
+  fa_status rc = bwd_setup(st, Q, K, V, dO, dK, dV, nullptr, B, H, N, d, causal, scale, kv_lens,
+                           workspace, workspace_bytes);
+  if (rc != FA_OK) return rc;
+  cudaError_t e = fa::launch_bwd_dkdv(d, /*with_dq=*/true, st.tq, st.tk, st.tv, st.tdo, st.tdk,
+                                      st.tdv, st.a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                               int B, int H, int N, int d, int causal, float scale,
+                               const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  fa_status rc = check_sizes(B, H, N, d);
+  if (rc != FA_OK) return rc;
+  if (!O || !LSE || !dQ || !aligned16(O)) return FA_ERR_INVALID_ARG;
+  BwdSetup st;
+  rc = bwd_setup(st, Q, K, V, dO, dK, dV, dQ, B, H, N, d, causal, scale, kv_lens, workspace,
+                 workspace_bytes);
+  if (rc != FA_OK) return rc;
+  const fa::Workspace w = fa::workspace_layout(B * H, N, d);
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_preprocess(
+      d, O, dO, LSE, B * H, N, reinterpret_cast<float*>(ws + w.neg_lse2_off),
+      reinterpret_cast<float*>(ws + w.neg_delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
+      /*zero_acc=*/false, s);
+  if (e == cudaSuccess)
+    e = fa::launch_bwd_dkdv(d, /*with_dq=*/false, st.tq, st.tk, st.tv, st.tdo, st.tdk, st.tdv,
+                            st.a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_dq(d, st.tq, st.tk, st.tv, st.tdo, st.tdq, st.a, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -74,7 +74,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              const float* __restrict__ lse, int N,
                                                              int nqt, float* __restrict__ neg_lse2,
                                                              float* __restrict__ neg_delta,
-                                                             float* __restrict__ dq_acc) {
+                                                             float* __restrict__ dq_acc,
+                                                             int zero_acc) {
   constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
   constexpr int RPW = 32 / G;  // rows per warp per pass
   const int i = blockIdx.x;
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       neg_delta[idx] = (q < N) ? -acc : 0.f;
     }
   }
+  if (!zero_acc) return;
   float4* t = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D);
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int idx = threadIdx.x; idx < 32 * D; idx += 256) t[idx] = z;
@@ -181,7 +183,9 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
 
 constexpr int kBwdThreads = 128 * (1 + kGroups);
 
-template <int D>
+// kWithDQ = false: the deterministic variant, dQ is computed by bwd_dq_kernel instead (no dQ
+// GEMM, no drain, no atomics, no dS copy in shared memory).
+template <int D, bool kWithDQ>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -344,10 +348,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ts(tmem + L::kColDK, tmem + L::kColDP + packed_col(kk), dq + kk * 128, idKV,
                  (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&q_empty[it & 1]);
+        if (kWithDQ) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
-          mma_ss(tmem + L::kColDP, desc_ds + kk * 128, desc_k + kk * 128, idQ, kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
+          for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
+            mma_ss(tmem + L::kColDP, desc_ds + kk * 128, desc_k + kk * 128, idQ, kk > 0 ? 1u : 0u);
+          mma_commit(dq_full);
+        }
       };
       auto wait_q = [&](int it) { return mbar_wait(&q_full[it & 1], (it >> 1) & 1, ctl); };
       auto wait_do = [&](int it) { return mbar_wait(&do_full[it & 1], (it >> 1) & 1, ctl); };
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl))) break;
           tc_fence_after();
           issue_dV(it + 1);
-          if (!(ok = wait_do(it + 1) && mbar_wait(dq_empty, it & 1, ctl))) break;
+          if (!(ok = wait_do(it + 1) && (!kWithDQ || mbar_wait(dq_empty, it & 1, ctl)))) break;
           tc_fence_after();
           issue_dP(it + 1);
           if (it + 2 < nI) {
@@ -485,7 +491,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
 
-      if (it > 0 && !(ok = drain(it - 1))) break;
+      if (kWithDQ && it > 0 && !(ok = drain(it - 1))) break;
 
       if (!(ok = mbar_wait_warp(dp_full, it & 1, ctl))) break;
       tc_fence_after();
@@ -512,21 +518,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         // dS^T packed over dP^T columns this group has already read (A operand of dK += dS^T Q)
         tmem_st16(tDP + 16 * c, ds);
-        // and to smem as [key row][query], 128-byte swizzled (A operand of dQ = dS K)
-        const int qa = q0 + 32 * c;  // absolute first query of this chunk
-        const uint32_t panel = sbase + L::kDS + (qa >> 6) * 16384;
+        if (kWithDQ) {  // and to smem as [key row][query], 128-byte swizzled (A of dQ = dS K)
+          const int qa = q0 + 32 * c;  // absolute first query of this chunk
+          const uint32_t panel = sbase + L::kDS + (qa >> 6) * 16384;
 #pragma unroll
-        for (int g = 0; g < 4; ++g)
-          st_shared_v4(panel + sw128_offset(r, ((qa & 63) >> 3) + g), ds[4 * g], ds[4 * g + 1],
-                       ds[4 * g + 2], ds[4 * g + 3]);
+          for (int g = 0; g < 4; ++g)
+            st_shared_v4(panel + sw128_offset(r, ((qa & 63) >> 3) + g), ds[4 * g], ds[4 * g + 1],
+                         ds[4 * g + 2], ds[4 * g + 3]);
+        }
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
+      if (kWithDQ) fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
     }
-    if (ok && nI > 0) ok = drain(nI - 1);
+    if (kWithDQ && ok && nI > 0) ok = drain(nI - 1);
 
     // ---- epilogue: the 64-column panels of dV and scale * dK (bf16, swizzled, over the V or K
     // tile in smem, which no MMA reads any more) are shared out over the groups; one TMA store
@@ -585,15 +592,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse, int BH,
                                   int N, float* neg_lse2, float* neg_delta, float* dq_acc,
-                                  cudaStream_t s) {
+                                  bool zero_acc, cudaStream_t s) {
   const int nqt = (N + 127) / 128;
   const dim3 grid(nqt, BH);
   auto o = static_cast<const __nv_bfloat16*>(O);
   auto g = static_cast<const __nv_bfloat16*>(dO);
   if (d == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc);
+    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc,
+                                                    zero_acc ? 1 : 0);
   else
-    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc);
+    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc,
+                                                     zero_acc ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -610,29 +619,32 @@ cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, 
 }
 
 namespace {
-template <int D>
+template <int D, bool kWithDQ>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                           BwdArgs a, cudaStream_t st) {
   using L = BwdLayout<D>;
   constexpr uint32_t kMaxSmem = 232448;  // 227 KB, the per-block opt-in limit of sm_100-family GPUs
   const uint32_t smem = (L::kBytes + 1024 <= kMaxSmem) ? L::kBytes + 1024 : kMaxSmem;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dkdv_kernel<D><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  bwd_dkdv_kernel<D, kWithDQ><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t s) {
-  if (d == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, tdk, tdv, a, s);
-  return launch_dkdv_d<128>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  if (d == 64)
+    return with_dq ? launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                   : launch_dkdv_d<64, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  return with_dq ? launch_dkdv_d<128, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                 : launch_dkdv_d<128, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
 }
 
 }  // namespace fa

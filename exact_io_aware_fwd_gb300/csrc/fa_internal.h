@@ -50,11 +50,16 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse,
                                   int BH, int N, float* neg_lse2, float* neg_delta, float* dq_acc,
-                                  cudaStream_t s);
-cudaError_t launch_bwd_dkdv(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                                  bool zero_acc, cudaStream_t s);
+// with_dq: accumulate dQ with atomics (fa_bwd); without: dK, dV only (deterministic path)
+cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
                             cudaStream_t s);
+// dQ by query tile, accumulated in tensor memory in a fixed order and stored as bf16
+cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                          const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N,
                                   float scale, cudaStream_t s);
 

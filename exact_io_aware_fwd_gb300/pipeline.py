@@ -53,9 +53,11 @@ class HostAttention:
         self.s_comp = torch.cuda.Stream(dev)
         self.s_out = torch.cuda.Stream(dev)
 
-    def run(self, q, k, v, do, causal=False, scale=None, kv_lens=None, out=None):
+    def run(self, q, k, v, do, causal=False, scale=None, kv_lens=None, out=None,
+            deterministic=False):
         """Host tensors in -> host tensors (O, LSE, dQ, dK, dV) out.  Inputs should be pinned
-        for the copies to overlap; outputs (``out``: dict of pinned tensors) are filled in place."""
+        for the copies to overlap; outputs (``out``: dict of pinned tensors) are filled in place.
+        ``deterministic`` runs the backward pass through fa_bwd_deterministic."""
         B, H, N, d = self.shape
         cur = torch.cuda.current_stream(self.device)
         if out is None:
@@ -81,10 +83,10 @@ class HostAttention:
                 o, lse = view(self.o), self.lse[sl]
                 binding.fa_fwd(view(self.q), view(self.k), view(self.v), causal=causal,
                                scale=scale, kv_lens=kv, out=o, lse=lse, stream=self.s_comp)
-                binding.fa_bwd(view(self.q), view(self.k), view(self.v), o, view(self.do), lse,
-                               causal=causal, scale=scale, kv_lens=kv, dq=view(self.dq),
-                               dk=view(self.dk), dv=view(self.dv),
-                               workspace=self.workspace, stream=self.s_comp)
+                bwd = binding.fa_bwd_deterministic if deterministic else binding.fa_bwd
+                bwd(view(self.q), view(self.k), view(self.v), o, view(self.do), lse,
+                    causal=causal, scale=scale, kv_lens=kv, dq=view(self.dq), dk=view(self.dk),
+                    dv=view(self.dv), workspace=self.workspace, stream=self.s_comp)
                 ev_comp = torch.cuda.Event()
                 ev_comp.record(self.s_comp)
             self.s_out.wait_event(ev_comp)

@@ -103,6 +103,21 @@ fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale,
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Deterministic backward pass: the arguments and results of fa_bwd, bit-for-bit reproducible from
+ * run to run.  dK and dV accumulate per key tile in tensor memory (as in fa_bwd); dQ is computed
+ * per query tile by a second kernel that recomputes S and dP and accumulates dQ over the key
+ * tiles in a fixed order, instead of fp32 atomics.  More work than fa_bwd (the deterministic
+ * option the pages describe for the official repository is likewise slower: page
+ * "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section "反向传播：用重计算代替存储").
+ * workspace: as for fa_bwd (its dQ accumulator is not used).
+ */
+fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                               int B, int H, int N, int d, int causal, float scale,
+                               const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/*
  * fa_bwd for callers that cannot allocate device memory.  The pages have no counterpart: this
  * entry point exists for callers with no device allocator to take the backward workspace from
  * (code running where cudaMalloc is forbidden or unsafe, such as host callbacks or allocator

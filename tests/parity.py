@@ -24,7 +24,8 @@ TOL_ZERO_GRAD = 1e-4  # absolute, where the exact gradient is identically zero
 ROW_CHUNK = 2048
 
 
-def run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd=True):
+def run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd=True, deterministic=False):
+    """fa_fwd (+ fa_bwd, or fa_bwd_deterministic) on cuda:0; returns device tensors."""
     import exact_io_aware_fwd_gb300 as fa
 
     dev = torch.device("cuda:0")
@@ -34,7 +35,8 @@ def run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd=True):
     out = {"O": o, "LSE": lse}
     if with_bwd:
         dod = do.to(dev)
-        dq, dk, dv = fa.fa_bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, kv_lens=kv)
+        bwd = fa.fa_bwd_deterministic if deterministic else fa.fa_bwd
+        dq, dk, dv = bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, kv_lens=kv)
         out.update(dQ=dq, dK=dk, dV=dv)
     st = fa.fa_get_error()
     assert st == fa.FA_OK, fa.fa_status_string(st)
@@ -110,11 +112,11 @@ def compare_slice(gpu_slice: dict, ref: dict, label: str, with_bwd=True, grad_to
 
 
 def check_case(q, k, v, do, causal, scale, kv_lens, slices=None, with_bwd=True, label="",
-               grad_tol=None):
+               grad_tol=None, deterministic=False):
     """Run the CUDA path on the whole batch and compare the chosen (b, h) slices."""
     B, H, N, d = q.shape
     sc = (1.0 / d ** 0.5) if scale is None else scale
-    out = run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd)
+    out = run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd, deterministic)
     torch.cuda.synchronize()
     slices = slices if slices is not None else [(b, h) for b in range(B) for h in range(H)]
     all_errs = []
