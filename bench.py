@@ -30,7 +30,8 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from exact_io_aware_fwd_gb300.workloads import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
+from exact_io_aware_fwd_gb300.workloads import (BY_NAME, HEADLINE, workload_block_mask,  # noqa: E402
+                                                 workload_inputs)
 
 METRIC = "attention fwd/bwd TFLOPS (bf16, 1\u00d7GB300) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -176,16 +177,24 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------- oracle timing
-def oracle_row_block(q, k, v, do, causal, scale, kv_len, rows):
+def oracle_row_block(q, k, v, do, causal, scale, kv_len, rows, block_mask=None):
     """One bounded sample of the oracle: forward + backward restricted to a block of query rows
     (O, LSE, D, dQ of those rows and their contributions to dK, dV).  Returns the credited
     FLOPs with the metric's convention: 14 d per visible (query, key) pair."""
     import oracle
 
-    st = oracle.row_statistics(q, k, v, do, scale, causal, kv_len, rows)
-    oracle.key_gradients(q, k, v, do, scale, st["LSE"], st["D"], causal, kv_len, rows=rows)
+    st = oracle.row_statistics(q, k, v, do, scale, causal, kv_len, rows, block_mask)
+    oracle.key_gradients(q, k, v, do, scale, st["LSE"], st["D"], causal, kv_len, rows=rows,
+                         block_mask=block_mask)
     n = k.shape[0]
     lim = n if kv_len is None else int(kv_len)
+    if block_mask is not None:
+        keys = np.arange(n)
+        vis = block_mask[(rows // 128)[:, None], (keys // 128)[None, :]] != 0
+        vis &= keys[None, :] < lim
+        if causal:
+            vis &= keys[None, :] <= rows[:, None]
+        return 14.0 * q.shape[1] * float(vis.sum())
     visible = np.minimum(rows + 1, lim) if causal else np.full(len(rows), lim)
     return 14.0 * q.shape[1] * float(visible.sum())
 
@@ -202,7 +211,9 @@ def cpu_sample_inputs(w, q, k, v, do, kv):
 def time_oracle_once(w, q, k, v, do, kv):
     qs, ks, vs, dos, kv_len, rows = cpu_sample_inputs(w, q, k, v, do, kv)
     t0 = time.perf_counter()
-    flops = oracle_row_block(qs, ks, vs, dos, w.causal, w.scale, kv_len, rows)
+    mask = workload_block_mask(w)
+    flops = oracle_row_block(qs, ks, vs, dos, w.causal, w.scale, kv_len, rows,
+                             None if mask is None else mask.numpy())
     dt = time.perf_counter() - t0
     return flops, dt, f"(b,h)=(0,0), query rows {rows[0]}..{rows[-1]} of N={w.N}: O, LSE, dQ and their dK, dV contributions"
 
@@ -234,7 +245,7 @@ def run_reference(args, w, world, rank):
         "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal},
+                   "causal": w.causal, "block_mask": w.block_mask},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -261,22 +272,34 @@ def run_ours(args, w, world, rank, local):
     f_fwd, f_bwd = w.flops()
 
     det = args.bwd == "deterministic"
-    stages = ["fwd", "bwd"] if det else ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    mask = workload_block_mask(w)
+    index = fa.fa_block_index_build(mask.to(dev), N) if mask is not None else None
+    two_stage = det or index is not None
+    stages = ["fwd", "bwd"] if two_stage else ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
 
-    def step_det(evs=None):
+    def step_two(evs=None):  # fa_fwd[_block_sparse], then one backward call
         if evs is not None:
             evs[0].record(stream)
-        fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
+        if index is not None:
+            fa.fa_fwd_block_sparse(qd, kd, vd, index, causal=w.causal, scale=w.scale,
+                                   kv_lens=kvd, out=o, lse=lse)
+        else:
+            fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
         if evs is not None:
             evs[1].record(stream)
-        fa.fa_bwd_deterministic(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale,
-                                kv_lens=kvd, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if index is not None:
+            fa.fa_bwd_block_sparse(qd, kd, vd, o, dod, lse, index, causal=w.causal,
+                                   scale=w.scale, kv_lens=kvd, deterministic=det, dq=dq, dk=dk,
+                                   dv=dv, workspace=ws)
+        else:
+            fa.fa_bwd_deterministic(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale,
+                                    kv_lens=kvd, dq=dq, dk=dk, dv=dv, workspace=ws)
         if evs is not None:
             evs[2].record(stream)
 
     def step(evs=None):
-        if det:
-            return step_det(evs)
+        if two_stage:
+            return step_two(evs)
         if evs is not None:
             evs[0].record(stream)
         fa.fa_fwd(qd, kd, vd, causal=w.causal, scale=w.scale, kv_lens=kvd, out=o, lse=lse)
@@ -339,7 +362,7 @@ def run_ours(args, w, world, rank, local):
 
         def e2e_step():
             ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout,
-                   deterministic=det)
+                   deterministic=det, block_index=index)
 
         for _ in range(2):
             e2e_step()
@@ -363,13 +386,13 @@ def run_ours(args, w, world, rank, local):
 
     # ---- roofline of the dominant kernel (largest share of the step)
     peaks, src = load_peaks()
-    bwd_stage = "bwd" if det else "bwd_dkdv"
+    bwd_stage = "bwd" if two_stage else "bwd_dkdv"
     dom = max(("fwd", bwd_stage), key=lambda s: stage_ms[s])
     dom_flops = f_fwd if dom == "fwd" else f_bwd
     achieved = dom_flops / (stage_ms[dom] * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
     kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel",
-                   "bwd": "bwd_dkdv_kernel+bwd_dq_kernel"}[dom]
+                   "bwd": "bwd_dkdv_kernel+bwd_dq_kernel" if det else "fa_bwd_block_sparse"}[dom]
     roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"bf16_tflops (burst) of {src}",
@@ -392,7 +415,8 @@ def run_ours(args, w, world, rank, local):
                    "kv_lens": None if kv is None else kv.tolist(),
                    "l2": "inputs larger than L2 (no flush)" if 4 * q.numel() * 2 > 129e6 else
                    "inputs smaller than L2 (not flushed)",
-                   "parallelism": f"replicas x{world}", "bwd": args.bwd},
+                   "parallelism": f"replicas x{world}", "bwd": args.bwd,
+                   "block_mask": w.block_mask},
         "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,

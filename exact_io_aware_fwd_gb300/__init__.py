@@ -13,9 +13,13 @@ from .binding import (  # noqa: F401
     FA_ERR_UNSUPPORTED,
     FA_ERR_WORKSPACE,
     FA_OK,
+    BlockIndex,
     FAError,
     default_scale,
+    fa_block_index_build,
+    fa_block_index_size,
     fa_bwd,
+    fa_bwd_block_sparse,
     fa_bwd_deterministic,
     fa_bwd_dkdv,
     fa_bwd_dq_convert,
@@ -23,6 +27,7 @@ from .binding import (  # noqa: F401
     fa_bwd_preprocess,
     fa_bwd_workspace_size,
     fa_fwd,
+    fa_fwd_block_sparse,
     fa_get_error,
     fa_status_string,
     load_library,

@@ -32,6 +32,10 @@ EXPORTED = [
     "fa_bwd_dq_convert",
     "fa_bwd_noalloc",
     "fa_bwd_deterministic",
+    "fa_block_index_size",
+    "fa_block_index_build",
+    "fa_fwd_block_sparse",
+    "fa_bwd_block_sparse",
     "fa_get_error",
     "fa_status_string",
 ]
@@ -72,6 +76,15 @@ def load_library(path: str | None = None):
     lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
                                           vp, vp, sz, vp]
     lib.fa_bwd_deterministic.restype = i
+    lib.fa_block_index_size.argtypes = [i, i]
+    lib.fa_block_index_size.restype = sz
+    lib.fa_block_index_build.argtypes = [vp, i, i, vp, sz, vp]
+    lib.fa_block_index_build.restype = i
+    lib.fa_fwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, vp, i, vp]
+    lib.fa_fwd_block_sparse.restype = i
+    lib.fa_bwd_block_sparse.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
+                                         vp, vp, i, i, vp, sz, vp]
+    lib.fa_bwd_block_sparse.restype = i
     lib.fa_get_error.argtypes = [vp]
     lib.fa_get_error.restype = i
     lib.fa_status_string.argtypes = [i]
@@ -231,3 +244,72 @@ def fa_get_error(stream=None) -> int:
 
 def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+class BlockIndex:
+    """Device block-sparse index built from a uint8 block mask over 128 x 128 tiles."""
+
+    def __init__(self, tensor, N, mask_heads):
+        self.tensor, self.N, self.mask_heads = tensor, N, mask_heads
+
+
+def fa_block_index_size(N, mask_heads=1) -> int:
+    return int(load_library().fa_block_index_size(int(N), int(mask_heads)))
+
+
+def fa_block_index_build(block_mask, N, stream=None) -> BlockIndex:
+    """Index of a [T, T] or [mask_heads, T, T] mask (T = ceil(N / 128), nonzero = kept)."""
+    if not block_mask.is_cuda:
+        raise ValueError("block_mask must be a CUDA tensor")
+    T = (int(N) + 127) // 128
+    m = block_mask.to(torch.uint8).contiguous()
+    if m.dim() == 2:
+        m = m[None]
+    if m.dim() != 3 or m.shape[1:] != (T, T):
+        raise ValueError(f"block_mask must be [T, T] or [heads, T, T] with T = {T}")
+    heads = m.shape[0]
+    nbytes = fa_block_index_size(N, heads)
+    idx = torch.empty(nbytes // 4, dtype=torch.int32, device=m.device)
+    st = load_library().fa_block_index_build(_ptr(m), int(N), heads, _ptr(idx), nbytes,
+                                             _stream(stream))
+    _check(st, "fa_block_index_build")
+    return BlockIndex(idx, int(N), heads)
+
+
+def fa_fwd_block_sparse(q, k, v, index: BlockIndex, causal=False, scale=None, kv_lens=None,
+                        out=None, lse=None, stream=None):
+    """fa_fwd restricted to the kept 128 x 128 tiles of `index` (see include/fa.h)."""
+    B, H, N, d = _check_qkv(q, k, v)
+    if index.N != N:
+        raise ValueError("block index built for another N")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
+                                            N, d, int(bool(causal)), _scale(scale), _ptr(kv),
+                                            _ptr(index.tensor), index.mask_heads, _stream(stream))
+    _check(st, "fa_fwd_block_sparse")
+    return out, lse
+
+
+def fa_bwd_block_sparse(q, k, v, o, do, lse, index: BlockIndex, causal=False, scale=None,
+                        kv_lens=None, deterministic=False, dq=None, dk=None, dv=None,
+                        workspace=None, stream=None):
+    """fa_bwd restricted to the kept tiles of `index` (see include/fa.h)."""
+    B, H, N, d = _check_qkv(q, k, v, o, do)
+    if index.N != N:
+        raise ValueError("block index built for another N")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace_for(q) if workspace is None else workspace
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
+                                            _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                            int(bool(causal)), _scale(scale), _ptr(kv),
+                                            _ptr(index.tensor), index.mask_heads,
+                                            int(bool(deterministic)), _ptr(ws), ws.numel(),
+                                            _stream(stream))
+    _check(st, "fa_bwd_block_sparse")
+    return dq, dk, dv
+

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libfa_sm103.so")
-SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_noalloc.cu"]
+SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_bwd.cu", "fa_bwd_dq.cu", "fa_block_sparse.cu", "fa_noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "sm103.cuh"), os.path.join(CSRC, "fa_internal.h"),
            os.path.join(ROOT, "include", "fa.h")]
 

@@ -122,8 +122,19 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   return fa::workspace_layout(B * H, N, d).total;
 }
 
-fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
-                 int N, int d, int causal, float scale, const int32_t* kv_lens, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fa_status check_block_index(const void* index, int mask_heads, int H) {
+  if (index == nullptr || (reinterpret_cast<uintptr_t>(index) & 15u) != 0) return FA_ERR_INVALID_ARG;
+  if (mask_heads != 1 && mask_heads != H) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                   int N, int d, int causal, float scale, const int32_t* kv_lens,
+                   const int32_t* blk, int blk_heads, void* stream) {
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
   if (!Q || !K || !V || !O || !LSE) return FA_ERR_INVALID_ARG;
@@ -152,11 +163,54 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
   a.scale_log2 = resolve_scale(scale, d) * kLog2e;
   a.kv_lens = kv_lens;
   a.lse = LSE;
+  a.blk = blk;
+  a.blk_heads = blk_heads;
   a.status = status;
   a.timeout_ns = wait_timeout_ns();
   if (static_cast<long long>(a.num_qblocks) * BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   cudaError_t e = fa::launch_fwd(d, tq, tk, tv, to, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H,
+                 int N, int d, int causal, float scale, const int32_t* kv_lens, void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens, nullptr, 1, stream);
+}
+
+size_t fa_block_index_size(int N, int mask_heads) {
+  if (N <= 0 || N > (1 << 30) || mask_heads <= 0 || mask_heads > 65535) return 0;
+  return static_cast<size_t>(mask_heads) *
+         static_cast<size_t>(fa::block_index_layout((N + 127) / 128).words) * sizeof(int32_t);
+}
+
+fa_status fa_block_index_build(const uint8_t* block_mask, int N, int mask_heads, void* index,
+                               size_t index_bytes, void* stream) {
+  if (block_mask == nullptr || index == nullptr) return FA_ERR_INVALID_ARG;
+  const size_t need = fa_block_index_size(N, mask_heads);
+  if (need == 0) return FA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(index) & 15u) != 0) return FA_ERR_INVALID_ARG;
+  if (index_bytes < need) return FA_ERR_WORKSPACE;
+  fa_status st = check_device();
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_block_index(block_mask, (N + 127) / 128, mask_heads,
+                                         static_cast<int32_t*>(index),
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_block_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const int32_t* kv_lens, const void* block_index, int mask_heads,
+                              void* stream) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_block_index(block_index, mask_heads, H)) != FA_OK) return st;
+  return fwd_impl(Q, K, V, O, LSE, B, H, N, d, causal, scale, kv_lens,
+                  static_cast<const int32_t*>(block_index), mask_heads, stream);
 }
 
 fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE, int B, int H, int N,
@@ -189,7 +243,8 @@ struct BwdSetup {
 
 fa_status bwd_setup(BwdSetup& st, const void* Q, const void* K, const void* V, const void* dO,
                     void* dK, void* dV, void* dQ, int B, int H, int N, int d, int causal,
-                    float scale, const int32_t* kv_lens, void* workspace, size_t workspace_bytes) {
+                    float scale, const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                    const int32_t* blk = nullptr, int blk_heads = 1) {
   fa_status rc = check_sizes(B, H, N, d);
   if (rc != FA_OK) return rc;
   if (!Q || !K || !V || !dO || !dK || !dV) return FA_ERR_INVALID_ARG;
@@ -221,6 +276,8 @@ fa_status bwd_setup(BwdSetup& st, const void* Q, const void* K, const void* V, c
   a.neg_lse2 = reinterpret_cast<const float*>(ws + w.neg_lse2_off);
   a.neg_delta = reinterpret_cast<const float*>(ws + w.neg_delta_off);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
+  a.blk = blk;
+  a.blk_heads = blk_heads;
   a.status = status;
   a.timeout_ns = wait_timeout_ns();
   if (static_cast<long long>(a.num_qtiles) * BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
@@ -244,17 +301,23 @@ fa_status fa_bwd_dkdv(const void* Q, const void* K, const void* V, const void* d
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, const void* O,
-                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                               int B, int H, int N, int d, int causal, float scale,
-                               const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
-                               void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Every backward entry point: preprocess, then either the dK/dV kernel with dQ atomics and the
+// dQ conversion, or (deterministic) the dK/dV kernel without dQ and the per-query-tile dQ kernel.
+fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                   const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
+                   int causal, float scale, const int32_t* kv_lens, void* workspace,
+                   size_t workspace_bytes, const int32_t* blk, int blk_heads, bool deterministic,
+                   void* stream) {
   fa_status rc = check_sizes(B, H, N, d);
   if (rc != FA_OK) return rc;
   if (!O || !LSE || !dQ || !aligned16(O)) return FA_ERR_INVALID_ARG;
   BwdSetup st;
   rc = bwd_setup(st, Q, K, V, dO, dK, dV, dQ, B, H, N, d, causal, scale, kv_lens, workspace,
-                 workspace_bytes);
+                 workspace_bytes, blk, blk_heads);
   if (rc != FA_OK) return rc;
   const fa::Workspace w = fa::workspace_layout(B * H, N, d);
   char* ws = static_cast<char*>(workspace);
@@ -262,12 +325,44 @@ fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, cons
   cudaError_t e = fa::launch_bwd_preprocess(
       d, O, dO, LSE, B * H, N, reinterpret_cast<float*>(ws + w.neg_lse2_off),
       reinterpret_cast<float*>(ws + w.neg_delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
-      /*zero_acc=*/false, s);
+      /*zero_acc=*/!deterministic, s);
   if (e == cudaSuccess)
-    e = fa::launch_bwd_dkdv(d, /*with_dq=*/false, st.tq, st.tk, st.tv, st.tdo, st.tdk, st.tdv,
-                            st.a, s);
-  if (e == cudaSuccess) e = fa::launch_bwd_dq(d, st.tq, st.tk, st.tv, st.tdo, st.tdq, st.a, s);
+    e = fa::launch_bwd_dkdv(d, /*with_dq=*/!deterministic, st.tq, st.tk, st.tv, st.tdo, st.tdk,
+                            st.tdv, st.a, s);
+  if (e == cudaSuccess) {
+    if (deterministic)
+      e = fa::launch_bwd_dq(d, st.tq, st.tk, st.tv, st.tdo, st.tdq, st.a, s);
+    else
+      e = fa::launch_bwd_dq_convert(d, st.a.dq_acc, dQ, B * H, N, st.a.scale, s);
+  }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, const void* O,
+                               const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                               int B, int H, int N, int d, int causal, float scale,
+                               const int32_t* kv_lens, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
+                  workspace_bytes, nullptr, 1, /*deterministic=*/true, stream);
+}
+
+fa_status fa_bwd_block_sparse(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const int32_t* kv_lens, const void* block_index, int mask_heads,
+                              int deterministic, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  fa_status rc = check_sizes(B, H, N, d);
+  if (rc != FA_OK) return rc;
+  if ((rc = check_block_index(block_index, mask_heads, H)) != FA_OK) return rc;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
+                  workspace_bytes, static_cast<const int32_t*>(block_index), mask_heads,
+                  deterministic != 0, stream);
 }
 
 fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, void* workspace,

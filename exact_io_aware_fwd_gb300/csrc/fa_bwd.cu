@@ -185,7 +185,9 @@ constexpr int kBwdThreads = 128 * (1 + kGroups);
 
 // kWithDQ = false: the deterministic variant, dQ is computed by bwd_dq_kernel instead (no dQ
 // GEMM, no drain, no atomics, no dS copy in shared memory).
-template <int D, bool kWithDQ>
+// kSparse: block-sparse; the key tile visits only the query tiles its mask column keeps (a
+// descending list from the block index, whose prefix of tiles >= the key tile is the causal part).
+template <int D, bool kWithDQ, bool kSparse>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -233,7 +235,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   int kv_len = N;
   if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
   const int i0 = a.causal ? j : 0;
-  const int nI = (j * 128 < kv_len) ? (nqt - i0) : 0;
+  int nI = (j * 128 < kv_len) ? (nqt - i0) : 0;  // query tiles this key tile visits
+  const int32_t* c_list = nullptr;
+  if constexpr (kSparse) {
+    const BlockIndex BI = block_index_layout(nqt);
+    const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bh % a.H) * BI.words);
+    c_list = base + BI.cidx + static_cast<int64_t>(j) * nqt;
+    nI = (j * 128 < kv_len) ? __ldg(base + (a.causal ? BI.cccnt : BI.ccnt) + j) : 0;
+  }
+  auto qtile = [&](int it) { return kSparse ? __ldg(c_list + it) : i0 + it; };
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -272,7 +282,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int nq = 0, ndo = 0;
       for (int it = 0; it < nI; ++it) {
-        const int i = i0 + it, s = it & 1;
+        const int i = qtile(it), s = it & 1;
         const uint32_t ph = (it >> 1) & 1;
         if (!mbar_wait(&q_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&q_full[s], L::kTile + 1024);
@@ -417,10 +427,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     // dQ_i (query row r of the tile, this group's columns) into the fp32 accumulator: load,
     // release the tensor memory (dP_{i+1} waits for it), then the atomics, which overlap dP_{i+1}
-    auto drain = [&](int it) -> bool {
+    auto drain = [&](int it, int qt) -> bool {  // qt: query tile of iteration it
       if (!mbar_wait_warp(dq_full, it & 1, ctl)) return false;
       tc_fence_after();
-      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + i0 + it) * 128 * D;
+      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + qt) * 128 * D;
       const int g0 = (kDC / 4) * grp;  // first 4-column group of this group's columns
       uint32_t va[32], vb[32];
       if (kDC >= 32) tmem_ld32(tDQ, va);
@@ -448,8 +458,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
 
     bool ok = true;
+    int i_prev = 0;  // query tile of the previous iteration (its dQ is drained in this one)
     for (int it = 0; it < nI; ++it) {
-      const int i = i0 + it, s = it & 1;
+      const int i = qtile(it), s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
       if (!(ok = mbar_wait_warp(&q_full[s], ph, ctl))) break;  // LSE and D are in smem
       if (!(ok = mbar_wait_warp(s_full, it & 1, ctl))) break;
@@ -491,7 +502,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
 
-      if (kWithDQ && it > 0 && !(ok = drain(it - 1))) break;
+      if (kWithDQ && it > 0 && !(ok = drain(it - 1, i_prev))) break;
 
       if (!(ok = mbar_wait_warp(dp_full, it & 1, ctl))) break;
       tc_fence_after();
@@ -532,8 +543,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
+      i_prev = i;
     }
-    if (kWithDQ && ok && nI > 0) ok = drain(nI - 1);
+    if (kWithDQ && ok && nI > 0) ok = drain(nI - 1, i_prev);
 
     // ---- epilogue: the 64-column panels of dV and scale * dK (bf16, swizzled, over the V or K
     // tile in smem, which no MMA reads any more) are shared out over the groups; one TMA store
@@ -619,20 +631,21 @@ cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, 
 }
 
 namespace {
-template <int D, bool kWithDQ>
+template <int D, bool kWithDQ, bool kSparse>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                           BwdArgs a, cudaStream_t st) {
   using L = BwdLayout<D>;
   constexpr uint32_t kMaxSmem = 232448;  // 227 KB, the per-block opt-in limit of sm_100-family GPUs
   const uint32_t smem = (L::kBytes + 1024 <= kMaxSmem) ? L::kBytes + 1024 : kMaxSmem;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ, kSparse>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dkdv_kernel<D, kWithDQ><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk, tdv, a);
+  bwd_dkdv_kernel<D, kWithDQ, kSparse><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk,
+                                                                        tdv, a);
   return cudaGetLastError();
 }
 }  // namespace
@@ -640,11 +653,18 @@ cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t s) {
+  if (a.blk != nullptr) {
+    if (d == 64)
+      return with_dq ? launch_dkdv_d<64, true, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                     : launch_dkdv_d<64, false, true>(tq, tk, tv, tdo, tdk, tdv, a, s);
+    return with_dq ? launch_dkdv_d<128, true, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                   : launch_dkdv_d<128, false, true>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  }
   if (d == 64)
-    return with_dq ? launch_dkdv_d<64, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                   : launch_dkdv_d<64, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
-  return with_dq ? launch_dkdv_d<128, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                 : launch_dkdv_d<128, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
+    return with_dq ? launch_dkdv_d<64, true, false>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                   : launch_dkdv_d<64, false, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  return with_dq ? launch_dkdv_d<128, true, false>(tq, tk, tv, tdo, tdk, tdv, a, s)
+                 : launch_dkdv_d<128, false, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
 }
 
 }  // namespace fa

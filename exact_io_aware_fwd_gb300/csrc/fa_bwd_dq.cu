@@ -16,6 +16,8 @@
 //   dP = dO_i V_j^T    (smem x smem)       -> tensor memory, two buffers [128, 256), [256, 384)
 //   dS = P o (dP - D_i), packed bf16 over the group's own dP columns
 //   dQ += dS K_j       (A = dS from tensor memory, B = K_j MN-major) -> [384, 384 + D)
+// Block-sparse (kSparse): the key tiles are the query tile's kept ones (an ascending list from the
+// block index, cut at the causal / key-length limit).
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -47,7 +49,8 @@ struct DqLayout {
   static constexpr int kNumBars = 17;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kBytes = kAbort + 4;
+  static constexpr uint32_t kCnt = kAbort + 4;  // block-sparse: key tiles to visit
+  static constexpr uint32_t kBytes = kCnt + 4;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 384;
   static constexpr uint32_t kTmemCols = 512;
 };
@@ -56,7 +59,20 @@ struct DqLayout {
 // the first half of its own 64 columns).
 __device__ __forceinline__ uint32_t dq_packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-template <int D>
+// Entries of the ascending list[0, cnt) below lim (whole warp).
+__device__ __forceinline__ int warp_count_below_dq(const int32_t* list, int cnt, int lim) {
+  int total = 0;
+  for (int c = 0; c < cnt; c += 32) {
+    const int idx = c + static_cast<int>(lane_id());
+    const bool ok = idx < cnt && __ldg(list + idx) < lim;
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    total += __popc(m);
+    if (m != 0xffffffffu) break;
+  }
+  return total;
+}
+
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -101,7 +117,19 @@ __global__ void __launch_bounds__(384, 1)
   if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
   int nkeys = kv_len;
   if (a.causal) nkeys = min(nkeys, i * 128 + 128);
-  const int nb = (nkeys + 127) / 128;  // key tiles 0 .. nb-1
+  const int nb_dense = (nkeys + 127) / 128;  // key tiles 0 .. nb_dense-1 are visible
+  const int32_t* r_list = nullptr;
+  int* cnt_smem = reinterpret_cast<int*>(sm + L::kCnt);
+  if constexpr (kSparse) {
+    const BlockIndex BI = block_index_layout(nqt);
+    const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bh % a.H) * BI.words);
+    r_list = base + BI.ridx + static_cast<int64_t>(i) * nqt;
+    if (warp == 2) {
+      const int c = warp_count_below_dq(r_list, __ldg(base + BI.rcnt + i), nb_dense);
+      if (lane == 0) *cnt_smem = c;
+    }
+  }
+  auto ktile = [&](int jj) { return kSparse ? __ldg(r_list + jj) : jj; };
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -125,6 +153,7 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(sm);
+  const int nb = kSparse ? *cnt_smem : nb_dense;  // key tiles this query tile visits
 
   if (warp == 0) {
     // ================= TMA producer
@@ -138,15 +167,16 @@ __global__ void __launch_bounds__(384, 1)
       for (int jj = 0; jj < nb; ++jj) {
         const int s = jj & 1;
         const uint32_t ph = (jj >> 1) & 1;
+        const int kt = ktile(jj);
         if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&k_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, jj * 128, bh);
+          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, kt * 128, bh);
         nk = jj + 1;
         if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&v_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, jj * 128, bh);
+          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, kt * 128, bh);
         nv = jj + 1;
       }
       if (*abort_flag) {
@@ -239,9 +269,10 @@ __global__ void __launch_bounds__(384, 1)
     const float2 nd = make_float2(ndl, ndl);
     bool ok = true;
     for (int jj = 0; jj < nb; ++jj) {
+      const int kt = ktile(jj);
       if (!(ok = mbar_wait_warp(s_full, jj & 1, ctl))) break;
       tc_fence_after();
-      const int k0 = jj * 128 + 64 * grp;  // first key of this group's columns
+      const int k0 = kt * 128 + 64 * grp;  // first key of this group's columns
       // keys >= klim are masked (causal: key > query; padding: key >= kv_len)
       const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;
       const bool masked = (k0 + 64 > klim);
@@ -342,7 +373,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool kSparse>
 cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, BwdArgs a,
                         cudaStream_t st) {
@@ -351,12 +382,13 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // tcgen05.alloc: ask for enough shared memory (d = 64 needs less than half an SM's) that one
   // CTA fills the SM.
   const uint32_t smem = L::kBytes + 1024 < 120u * 1024u ? 120u * 1024u : L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, kSparse>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dq_kernel<D><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_dq_kernel<D, kSparse><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -365,8 +397,12 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const BwdArgs& a, cudaStream_t s) {
-  if (d == 64) return launch_dq_d<64>(tq, tk, tv, tdo, tdq, a, s);
-  return launch_dq_d<128>(tq, tk, tv, tdo, tdq, a, s);
+  if (a.blk != nullptr) {
+    if (d == 64) return launch_dq_d<64, true>(tq, tk, tv, tdo, tdq, a, s);
+    return launch_dq_d<128, true>(tq, tk, tv, tdo, tdq, a, s);
+  }
+  if (d == 64) return launch_dq_d<64, false>(tq, tk, tv, tdo, tdq, a, s);
+  return launch_dq_d<128, false>(tq, tk, tv, tdo, tdq, a, s);
 }
 
 }  // namespace fa

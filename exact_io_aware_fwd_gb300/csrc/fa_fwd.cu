@@ -24,6 +24,10 @@
 //    (page two, FlashAttention-1 section, causal paragraph).
 //  * epilogue: O~ / l -> bf16 -> swizzled smem (over the Q tile) -> TMA store (rows >= N are
 //    clipped by the tensor map); LSE with plain coalesced stores.
+//  * block-sparse (kSparse): the K/V stream is the union of the kept key tiles of the CTA's two
+//    query tiles (a sorted list from the block index); each query tile runs S, softmax and P V
+//    only on its own kept tiles, so skipped tiles cost neither loads nor MMAs (page two,
+//    FlashAttention-1 section: the block-sparse extension skips zero blocks).
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -59,7 +63,8 @@ struct FwdLayout {
   static constexpr int kNumBars = 1 + 4 * kStages + 7;
   static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
-  static constexpr uint32_t kBytes = kAbort + 4;
+  static constexpr uint32_t kCnt = kAbort + 4;  // block-sparse counts: positions, n_0, n_1
+  static constexpr uint32_t kBytes = kCnt + 12;
   // TMEM columns: S_0, S_1 (128 each), O_0, O_1 (D each)
   static constexpr uint32_t kColS0 = 0, kColO0 = 256;
   static constexpr uint32_t kTmemCols = 512;
@@ -78,7 +83,21 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
   }
 }
 
-template <int D>
+// Number of entries of the ascending list[0, cnt) below lim (whole warp; a sorted list fails the
+// test only after its last passing entry).
+__device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, int lim) {
+  int total = 0;
+  for (int c = 0; c < cnt; c += 32) {
+    const int idx = c + static_cast<int>(lane_id());
+    const bool ok = idx < cnt && __ldg(list + idx) < lim;
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    total += __popc(m);
+    if (m != 0xffffffffu) break;
+  }
+  return total;
+}
+
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -136,6 +155,34 @@ __global__ void __launch_bounds__(384, 1)
     nb[t] = (qt0 < N) ? (nkeys + 127) / 128 : 0;
   }
   const int nb_max = max(nb[0], nb[1]);
+  const int T = (N + 127) / 128;
+
+  // block-sparse: the CTA's K/V stream (f_list) and each query tile's key tiles (r_list) come
+  // from the block index, cut at the causal / key-length limits nb[]
+  const int32_t* f_list = nullptr;
+  const int32_t* r_list[2] = {nullptr, nullptr};
+  int* cnt_smem = reinterpret_cast<int*>(sm + L::kCnt);
+  if constexpr (kSparse) {
+    const BlockIndex BI = block_index_layout(T);
+    const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bh % a.H) * BI.words);
+    f_list = base + BI.fidx + static_cast<int64_t>(qb) * T;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+      if (2 * qb + t < T) r_list[t] = base + BI.ridx + static_cast<int64_t>(2 * qb + t) * T;
+    if (warp == 2) {
+      const int np = warp_count_below(f_list, __ldg(base + BI.fcnt + qb), nb_max * 4);
+      int nt[2] = {0, 0};
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (r_list[t] != nullptr)
+          nt[t] = warp_count_below(r_list[t], __ldg(base + BI.rcnt + 2 * qb + t), nb[t]);
+      if (lane == 0) {
+        cnt_smem[0] = np;
+        cnt_smem[1] = nt[0];
+        cnt_smem[2] = nt[1];
+      }
+    }
+  }
 
   // ---- setup
   if (warp == 0 && lane == 0) {
@@ -168,10 +215,13 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(sm);
+  // positions of the K/V stream and key tiles per query tile
+  const int npos = kSparse ? cnt_smem[0] : nb_max;
+  const int ncnt[2] = {kSparse ? cnt_smem[1] : nb[0], kSparse ? cnt_smem[2] : nb[1]};
 
   if (warp == 0) {
     // ================= TMA producer
-    if (lane == 0 && nb_max > 0) {
+    if (lane == 0 && npos > 0) {
       const int ntiles = (nb[1] > 0) ? 2 : 1;
       mbar_arrive_expect_tx(q_full, ntiles * L::kTile);
       for (int t = 0; t < ntiles; ++t)
@@ -179,19 +229,20 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64, q0 + 128 * t,
                       bh);
       int jk = 0, jv = 0;  // K and V tiles whose copies have been issued
-      for (int j = 0; j < nb_max; ++j) {
+      for (int j = 0; j < npos; ++j) {
         const int s = j % S;
         const uint32_t ph = (j / S) & 1;
+        const int kt = kSparse ? (__ldg(f_list + j) >> 2) : j;  // key tile at position j
         if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&k_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, j * 128,
+          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, kt * 128,
                       bh);
         jk = j + 1;
         if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&v_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, j * 128,
+          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, kt * 128,
                       bh);
         jv = j + 1;
       }
@@ -204,47 +255,73 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ================= MMA issuer
-    if (lane == 0 && nb_max > 0) {
+    if (lane == 0 && npos > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S = Q K^T, both K-major
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);     // O += P V, V is MN-major
       bool ok = mbar_wait(q_full, 0, ctl);
-      for (int j = 0; ok && j <= nb_max; ++j) {
+      int cnt[2] = {0, 0};     // S MMAs issued per query tile
+      uint32_t use_prev = 0;   // bit t: query tile t used the previous position
+      for (int j = 0; ok && j <= npos; ++j) {
         const int s = j % S;
         const int sp = (j + S - 1) % S;
-        if (j < nb_max && !(ok = mbar_wait(&k_full[s], (j / S) & 1, ctl))) break;
+        uint32_t use = 0;  // bit t: query tile t uses position j
+        if (j < npos) {
+          if constexpr (kSparse) {
+            const int e = __ldg(f_list + j);
+            const int kt = e >> 2;
+            use = (((e & 1) && kt < nb[0]) ? 1u : 0u) | (((e & 2) && kt < nb[1]) ? 2u : 0u);
+          } else {
+            use = (j < nb[0] ? 1u : 0u) | (j < nb[1] ? 2u : 0u);
+          }
+        }
+        if (j < npos && !(ok = mbar_wait(&k_full[s], (j / S) & 1, ctl))) break;
         if (j >= 1 && !(ok = mbar_wait(&v_full[sp], ((j - 1) / S) & 1, ctl))) break;
         tc_fence_after();
+        const uint32_t qbs0 = sbase + L::kQ;
+        const uint32_t kbs = sbase + L::kK + s * L::kTile;
+        auto issue_S = [&](int t) {  // S_t = Q_t K_j^T
+          const uint32_t qbs = qbs0 + t * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            const uint64_t adesc = sdesc_sw128(qbs + off, 16384, 1024);
+            const uint64_t bdesc = sdesc_sw128(kbs + off, 16384, 1024);
+            mma_ss(tmem + L::kColS0 + 128 * t, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[t]);
+          ++cnt[t];
+        };
+        // Block-sparse: S of a tile that starts a use here with no P V pending needs no softmax
+        // result, so it goes first and the other tile's softmax overlaps it.  (In the dense
+        // stream every position after the first continues both tiles: the plain order below.)
+        if constexpr (kSparse) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (((use >> t) & 1u) && !((use_prev >> t) & 1u)) issue_S(t);
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const uint32_t colS = L::kColS0 + 128 * t;
-          const uint32_t colO = L::kColO0 + D * t;
-          if (j >= 1 && j - 1 < nb[t]) {
-            if (!(ok = mbar_wait(&p_full[t], (j - 1) & 1, ctl))) break;
+          if ((use_prev >> t) & 1u) {
+            if (!(ok = mbar_wait(&p_full[t], (cnt[t] - 1) & 1, ctl))) break;
             tc_fence_after();
             const uint32_t vb = sbase + L::kV + sp * L::kTile;
+            const uint32_t colS = L::kColS0 + 128 * t;
+            const uint32_t colO = L::kColO0 + D * t;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA; P packed 2 per column
               const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-              mma_ts(tmem + colO, tmem + colS + kk * 8, bdesc, idO, (j > 1 || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + colO, tmem + colS + kk * 8, bdesc, idO,
+                     (cnt[t] > 1 || kk > 0) ? 1u : 0u);
             }
-            if (j - 1 == nb[t] - 1) mma_commit(&o_full[t]);
+            if (cnt[t] == ncnt[t]) mma_commit(&o_full[t]);  // the tile's last P V
           }
-          if (j < nb[t]) {
-            const uint32_t qbs = sbase + L::kQ + t * L::kTile;
-            const uint32_t kbs = sbase + L::kK + s * L::kTile;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              const uint64_t adesc = sdesc_sw128(qbs + off, 16384, 1024);
-              const uint64_t bdesc = sdesc_sw128(kbs + off, 16384, 1024);
-              mma_ss(tmem + colS, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
-            }
-            mma_commit(&s_full[t]);
-          }
+          // S_t overwrites P_t: after the tile's own P V
+          if (((use >> t) & 1u) && (!kSparse || ((use_prev >> t) & 1u))) issue_S(t);
         }
         if (!ok) break;
-        if (j < nb_max) mma_commit(&k_empty[s]);
+        if (j < npos) mma_commit(&k_empty[s]);
         if (j >= 1) mma_commit(&v_empty[sp]);
+        use_prev = use;
       }
       // every MMA issued by this thread has finished before tensor memory is released
       mma_commit(mma_done);
@@ -261,12 +338,15 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tmem + lanes + L::kColS0 + 128 * t;
     const uint32_t tO = tmem + lanes + L::kColO0 + D * t;
     const float c2 = a.scale_log2;
-    const int n = nb[t];
+    const int n = ncnt[t];
+    int kt_next = (kSparse && n > 0) ? __ldg(r_list[t]) : 0;
     float m_run = -INFINITY;  // running max of scale*log2(e)*s (log2 units)
     float l_run = 0.f;        // running sum of exp2(. - m_run)
     float lr_run = 0.f;       // the same sum over the bf16-rounded values (normalises O~)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
+      const int kt = kSparse ? kt_next : j;  // key tile of this query tile's j-th S
+      if (kSparse && j + 1 < n) kt_next = __ldg(r_list[t] + j + 1);
       if (!(ok = mbar_wait_warp(&s_full[t], j & 1, ctl))) break;
       tc_fence_after();
       uint32_t s[128];
@@ -276,7 +356,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_wait_ld();
       reg_fence(s);
-      const int k0 = j * 128;
+      const int k0 = kt * 128;
       const bool masked = (k0 + 128 > kv_len) || (a.causal && k0 == qt0);
       const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;  // keys < klim are visible
       // row max: 3-input max over 4 independent chains (a single chain is 128 dependent steps)
@@ -367,6 +447,9 @@ __global__ void __launch_bounds__(384, 1)
     // ---- epilogue: O = O~ / l -> bf16 -> swizzled smem over Q_t -> TMA store; LSE
     const bool tile_live = (qt0 < N);
     if (ok && n > 0) ok = mbar_wait_warp(&o_full[t], 0, ctl);
+    // block-sparse: a tile with no kept key tile still had its Q copied in (for the other tile's
+    // sake); that copy must land before the staging below reuses its shared memory
+    if (kSparse && ok && n == 0 && npos > 0) ok = mbar_wait_warp(q_full, 0, ctl);
     if (tile_live) {  // uniform over the warpgroup
       if (ok) {
         tc_fence_after();
@@ -420,17 +503,18 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool kSparse>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, FwdArgs a, cudaStream_t st) {
   using L = FwdLayout<D>;
   const uint32_t smem = L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kSparse>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qblocks) * static_cast<unsigned>(a.BH);
-  fwd_kernel<D><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
+  fwd_kernel<D, kSparse><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -438,8 +522,12 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t s) {
-  if (d == 64) return launch_fwd_d<64>(tq, tk, tv, to, a, s);
-  return launch_fwd_d<128>(tq, tk, tv, to, a, s);
+  if (a.blk != nullptr) {
+    if (d == 64) return launch_fwd_d<64, true>(tq, tk, tv, to, a, s);
+    return launch_fwd_d<128, true>(tq, tk, tv, to, a, s);
+  }
+  if (d == 64) return launch_fwd_d<64, false>(tq, tk, tv, to, a, s);
+  return launch_fwd_d<128, false>(tq, tk, tv, to, a, s);
 }
 
 }  // namespace fa

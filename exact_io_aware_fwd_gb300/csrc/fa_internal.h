@@ -10,6 +10,31 @@ namespace fa {
 
 constexpr int kTileRows = 128;  // query rows per Q tile and keys per K/V tile
 
+// Block-sparse index: the lists of kept 128 x 128 tiles that the kernels walk, built on the
+// device from a uint8 block mask [T][T] (T = ceil(N / 128)).  int32 words per mask head:
+//   fcnt[Tb]     positions of the shared K/V stream of each 256-row query block (Tb = ceil(T/2))
+//   fidx[Tb][T]  key tile * 4 + 1 (kept by the block's first query tile) + 2 (by its second)
+//   rcnt[T]      kept key tiles of each query tile;  ridx[T][T]  those key tiles, ascending
+//   ccnt[T]      kept query tiles of each key tile;  cccnt[T]  how many of them are >= the key
+//                tile (the causal prefix);  cidx[T][T]  those query tiles, descending
+// Sorted lists let a kernel cut them at a key-length or causal limit by counting a prefix.
+struct BlockIndex {
+  int64_t fcnt, fidx, rcnt, ridx, ccnt, cccnt, cidx, words;
+};
+__host__ __device__ inline BlockIndex block_index_layout(int T) {
+  BlockIndex L;
+  const int64_t t = T, tb = (T + 1) / 2;
+  L.fcnt = 0;
+  L.fidx = L.fcnt + tb;
+  L.rcnt = L.fidx + tb * t;
+  L.ridx = L.rcnt + t;
+  L.ccnt = L.ridx + t * t;
+  L.cccnt = L.ccnt + t;
+  L.cidx = L.cccnt + t;
+  L.words = L.cidx + t * t;
+  return L;
+}
+
 // Forward kernel arguments (tensor maps travel separately as __grid_constant__ parameters).
 struct FwdArgs {
   int H, N, BH;
@@ -19,6 +44,8 @@ struct FwdArgs {
   float scale_log2;       // scale * log2(e)
   const int32_t* kv_lens; // device int32[B] or nullptr
   float* lse;             // [B, H, N] fp32
+  const int32_t* blk;     // block-sparse index (BlockIndex layout) or nullptr for dense
+  int blk_heads;          // mask heads in blk: 1 (shared by every head) or H
   int* status;            // library status word (device)
   uint64_t timeout_ns;    // limit of a single pipeline wait
   uint32_t smem_bytes;    // dynamic shared memory actually granted
@@ -34,6 +61,8 @@ struct BwdArgs {
   const float* neg_lse2;  // workspace: -LSE * log2(e), [BH][Npad], -inf on padded rows
   const float* neg_delta; // workspace: -D = -rowsum(dO o O), [BH][Npad], 0 on padded rows
   float* dq_acc;          // workspace: dQ accumulator, tile-major (see fa_bwd.cu)
+  const int32_t* blk;     // block-sparse index or nullptr (as in FwdArgs)
+  int blk_heads;
   int* status;
   uint64_t timeout_ns;
   uint32_t smem_bytes;
@@ -60,6 +89,9 @@ cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CU
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const BwdArgs& a, cudaStream_t s);
+// block-sparse index of mask_heads masks [T][T] into `index` (mask_heads * words int32)
+cudaError_t launch_block_index(const uint8_t* mask, int T, int mask_heads, int32_t* index,
+                               cudaStream_t s);
 cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N,
                                   float scale, cudaStream_t s);
 

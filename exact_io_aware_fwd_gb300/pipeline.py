@@ -54,11 +54,14 @@ class HostAttention:
         self.s_out = torch.cuda.Stream(dev)
 
     def run(self, q, k, v, do, causal=False, scale=None, kv_lens=None, out=None,
-            deterministic=False):
+            deterministic=False, block_index=None):
         """Host tensors in -> host tensors (O, LSE, dQ, dK, dV) out.  Inputs should be pinned
         for the copies to overlap; outputs (``out``: dict of pinned tensors) are filled in place.
-        ``deterministic`` runs the backward pass through fa_bwd_deterministic."""
+        ``deterministic`` runs the backward pass through fa_bwd_deterministic; ``block_index``
+        (a binding.BlockIndex with one mask shared by all heads) runs the block-sparse calls."""
         B, H, N, d = self.shape
+        if block_index is not None and block_index.mask_heads != 1:
+            raise ValueError("the host pipeline takes a block mask shared by every head")
         cur = torch.cuda.current_stream(self.device)
         if out is None:
             out = {name: torch.empty(self.shape, dtype=torch.bfloat16).pin_memory()
@@ -81,12 +84,21 @@ class HostAttention:
                 view = lambda t: t[sl]  # noqa: E731  [b1-b0, h1-h0, N, d], contiguous
                 kv = self.kv[b0:b1] if kv_lens is not None else None
                 o, lse = view(self.o), self.lse[sl]
-                binding.fa_fwd(view(self.q), view(self.k), view(self.v), causal=causal,
-                               scale=scale, kv_lens=kv, out=o, lse=lse, stream=self.s_comp)
-                bwd = binding.fa_bwd_deterministic if deterministic else binding.fa_bwd
-                bwd(view(self.q), view(self.k), view(self.v), o, view(self.do), lse,
-                    causal=causal, scale=scale, kv_lens=kv, dq=view(self.dq), dk=view(self.dk),
-                    dv=view(self.dv), workspace=self.workspace, stream=self.s_comp)
+                qkv = (view(self.q), view(self.k), view(self.v))
+                grads = dict(dq=view(self.dq), dk=view(self.dk), dv=view(self.dv),
+                             workspace=self.workspace, stream=self.s_comp)
+                if block_index is not None:
+                    binding.fa_fwd_block_sparse(*qkv, block_index, causal=causal, scale=scale,
+                                                kv_lens=kv, out=o, lse=lse, stream=self.s_comp)
+                    binding.fa_bwd_block_sparse(*qkv, o, view(self.do), lse, block_index,
+                                                causal=causal, scale=scale, kv_lens=kv,
+                                                deterministic=deterministic, **grads)
+                else:
+                    binding.fa_fwd(*qkv, causal=causal, scale=scale, kv_lens=kv, out=o, lse=lse,
+                                   stream=self.s_comp)
+                    bwd = binding.fa_bwd_deterministic if deterministic else binding.fa_bwd
+                    bwd(*qkv, o, view(self.do), lse, causal=causal, scale=scale, kv_lens=kv,
+                        **grads)
                 ev_comp = torch.cuda.Event()
                 ev_comp.record(self.s_comp)
             self.s_out.wait_event(ev_comp)

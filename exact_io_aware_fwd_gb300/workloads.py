@@ -9,6 +9,13 @@ Recipe (one generator per workload, ``torch.Generator().manual_seed(seed)`` on t
   2. if the workload has key padding, ``kv_lens = torch.randint(lo, hi + 1, (B,))`` is drawn
      next from the same generator.
 Layout: contiguous [B, H, N, d] bfloat16, the order the attention signature uses.
+
+Block-sparse workloads add a block mask over 128 x 128 tiles (uint8 [T, T], T = ceil(N / 128),
+nonzero = kept), shared by every batch and head.  The pages name a fixed butterfly pattern for
+the block-sparse extension without drawing it; ``butterfly_block_mask`` takes the support of the
+butterfly factors: tile (i, j) is kept when i and j differ in at most one bit, so every row keeps
+its diagonal tile and the tiles at distance 2^k in the butterfly sense (1 + log2 T per row when T
+is a power of two).
 """
 
 from __future__ import annotations
@@ -31,6 +38,7 @@ class Workload:
     sigma_vdo: float = 1.0
     kv_len_range: tuple | None = None  # inclusive (lo, hi) of per-batch key lengths
     oracle_slices: int = 0  # (batch, head) slices the oracle checks at full size (0 = all)
+    block_mask: str | None = None  # "butterfly": block-sparse over 128 x 128 tiles
     notes: str = field(default="", compare=False)
 
     @property
@@ -38,7 +46,18 @@ class Workload:
         return 1.0 / float(self.d) ** 0.5
 
     def flops(self) -> tuple[float, float]:
-        """(forward, backward) FLOPs: 4 N^2 d and 10 N^2 d per head, halved when causal."""
+        """(forward, backward) FLOPs: 4 N^2 d and 10 N^2 d per head, halved when causal.  With a
+        block mask N^2 becomes the area of the kept tiles (a causal diagonal tile counts half)."""
+        if self.block_mask is not None:
+            bm = workload_block_mask(self).bool()
+            t = bm.shape[0]
+            sizes = torch.tensor([min(128, self.N - 128 * i) for i in range(t)], dtype=torch.float64)
+            area = sizes[:, None] * sizes[None, :]
+            if self.causal:
+                area = torch.where(torch.eye(t, dtype=torch.bool), area / 2, area)
+                bm = bm & torch.tril(torch.ones(t, t, dtype=torch.bool))
+            per_head = float((area * bm).sum()) * self.d
+            return 4.0 * per_head * self.B * self.H, 10.0 * per_head * self.B * self.H
         per_head = float(self.N) * self.N * self.d
         f = 4.0 * per_head * self.B * self.H
         b = 10.0 * per_head * self.B * self.H
@@ -59,7 +78,14 @@ WORKLOADS = [
              kv_len_range=(1000, 2000), oracle_slices=8),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Block-sparse: the long-context shape, non-causal, with the butterfly block mask (8 of 128
+# tiles per row, 6.25% of the dense work).
+SPARSE_WORKLOADS = [
+    Workload("butterfly-1x32x16384x128", 1, 32, 16384, 128, False, seed=5, oracle_slices=2,
+             block_mask="butterfly"),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + SPARSE_WORKLOADS}
 HEADLINE = WORKLOADS[3]
 
 
@@ -101,3 +127,26 @@ def sample_slices(w: Workload, count=None, seed_offset=1000):
         return [(b, h) for b, h in enumerate(heads)]
     picks = torch.randperm(total, generator=g)[:count].tolist()
     return [(bh // w.H, bh % w.H) for bh in sorted(picks)]
+
+
+def butterfly_block_mask(T: int) -> torch.Tensor:
+    """uint8 [T, T]: tile (i, j) kept when i XOR j has at most one bit set."""
+    i = torch.arange(T)
+    x = i[:, None] ^ i[None, :]
+    return ((x & (x - 1)) == 0).to(torch.uint8)
+
+
+def random_block_mask(T: int, density: float, seed: int, heads: int = 1) -> torch.Tensor:
+    """uint8 [heads, T, T] (or [T, T] for heads == 1), each tile kept with probability density."""
+    g = torch.Generator().manual_seed(int(seed))
+    m = (torch.rand((heads, T, T), generator=g) < density).to(torch.uint8)
+    return m[0] if heads == 1 else m
+
+
+def workload_block_mask(w: Workload) -> torch.Tensor | None:
+    if w.block_mask is None:
+        return None
+    if w.block_mask == "butterfly":
+        return butterfly_block_mask((w.N + 127) // 128)
+    raise ValueError(f"unknown block mask {w.block_mask!r}")
+

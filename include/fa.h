@@ -118,6 +118,46 @@ fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, cons
                                void* stream);
 
 /*
+ * Block-sparse attention.  A block mask over tiles of 128 queries x 128 keys keeps or drops
+ * whole tiles: the scores of query i and key j count only where
+ * block_mask[i / 128][j / 128] != 0 (and the causal and key-length masks keep them too); the
+ * kernels skip dropped tiles entirely, so work and HBM traffic scale with the kept fraction s,
+ * and the result is exact attention under that mask.  Cite: page "FlashAttention 入门：从 FA1 到
+ * FA4 的 IO 感知注意力", section "FlashAttention-1：分块与在线 softmax" (the block-sparse
+ * extension skips zero blocks, exact within the kept ones); first page, section "IO 复杂度、
+ * 内存复杂度与 exactness 的边界" (HBM accesses Theta(Nd + N^2 d^2 s / M)).
+ *
+ * Use: build the block index once per mask with fa_block_index_build, then pass it to any
+ * number of fa_fwd_block_sparse / fa_bwd_block_sparse calls with the same N.
+ *
+ * fa_block_index_size: bytes of the index for sequence length N and mask_heads masks
+ *   (12 * T^2 + 12 * T bytes per mask, T = ceil(N / 128)); 0 for invalid sizes.
+ * fa_block_index_build: block_mask is DEVICE uint8 [mask_heads][T][T], row = query tile,
+ *   column = key tile, nonzero = kept.  index: DEVICE memory of at least
+ *   fa_block_index_size(N, mask_heads) bytes, 16-byte aligned, owned by the caller; it holds the
+ *   sorted lists of kept tiles the kernels walk.  Asynchronous on `stream`; the mask may be
+ *   freed or changed once the build has run.  FA_ERR_WORKSPACE if index_bytes is too small.
+ * fa_fwd_block_sparse / fa_bwd_block_sparse: the arguments and results of fa_fwd / fa_bwd (the
+ *   backward with the same workspace) plus block_index (built for this N) and mask_heads: 1
+ *   (one mask shared by every batch and head) or H (mask h for head h of every batch).
+ *   deterministic != 0 makes the backward bit-reproducible as fa_bwd_deterministic does.  A
+ *   query row that keeps no visible key gets O = 0, LSE = -inf and zero gradients.
+ */
+size_t fa_block_index_size(int N, int mask_heads);
+fa_status fa_block_index_build(const uint8_t* block_mask, int N, int mask_heads, void* index,
+                               size_t index_bytes, void* stream);
+fa_status fa_fwd_block_sparse(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const int32_t* kv_lens, const void* block_index, int mask_heads,
+                              void* stream);
+fa_status fa_bwd_block_sparse(const void* Q, const void* K, const void* V, const void* O,
+                              const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                              int B, int H, int N, int d, int causal, float scale,
+                              const int32_t* kv_lens, const void* block_index, int mask_heads,
+                              int deterministic, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
  * fa_bwd for callers that cannot allocate device memory.  The pages have no counterpart: this
  * entry point exists for callers with no device allocator to take the backward workspace from
  * (code running where cudaMalloc is forbidden or unsafe, such as host callbacks or allocator

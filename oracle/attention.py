@@ -21,8 +21,17 @@ Masks (both written as score = -inf, i.e. probability exactly 0):
   section "FlashAttention-1：分块与在线 softmax", paragraph on causal masking: skip blocks j > i);
 * key padding: key j >= kv_len is masked (first page, 使用契约 table row "mask/dropout").
 
-A row with no unmasked key (only reachable with kv_len == 0) has O = 0, LSE = -inf and zero
-gradients; this convention is the oracle's own, the pages do not define it.
+* block mask (block-sparse attention): the scores of query i and key j are kept only where
+  block_mask[i // block, j // block] is nonzero, every other score is masked.  The extension
+  skips the zero blocks and stays exact inside the kept ones (page "FlashAttention 入门：从 FA1
+  到 FA4 的 IO 感知注意力", section "FlashAttention-1：分块与在线 softmax", paragraph after the
+  causal note; first page, sections "作者团队与论文的系统研究脉络" and "IO 复杂度、内存复杂度与
+  exactness 的边界", IO = Theta(Nd + N^2 d^2 s / M) for a fraction s of nonzero blocks).  The
+  masks combine: an entry counts only if every mask keeps it.
+
+A row with no unmasked key (reachable with kv_len == 0, or a block mask whose row keeps no
+visible block) has O = 0, LSE = -inf and zero gradients; this convention is the oracle's own,
+the pages do not define it.
 
 The second forward route, ``tiled_forward``, restates the pages' online-softmax recurrence
 (running max m, running sum l, unnormalised output O~, one final divide) in the order the
@@ -54,25 +63,33 @@ def _f64(x):
     return np.asarray(x, dtype=np.float64)
 
 
-def masked_scores(q, k, scale, causal=False, kv_len=None, rows=None):
+def _mask(rows, keys, causal, kv_len, block_mask, block):
+    """Boolean [len(rows), len(keys)]: True where the score of (row, key) is masked."""
+    masked = np.zeros((rows.shape[0], keys.shape[0]), dtype=bool)
+    if causal:
+        masked |= keys[None, :] > rows[:, None]
+    if kv_len is not None:
+        masked |= keys[None, :] >= int(kv_len)
+    if block_mask is not None:
+        bm = np.asarray(block_mask) != 0
+        masked |= ~bm[(rows // block)[:, None], (keys // block)[None, :]]
+    return masked
+
+
+def masked_scores(q, k, scale, causal=False, kv_len=None, rows=None, block_mask=None, block=128):
     """S[rows, :] = scale * Q[rows] K^T with masked entries set to -inf.
 
     q: [N_q, d], k: [N_k, d].  ``rows`` selects query rows (default: all); the causal mask
     compares the key index with the *absolute* query index, so a row subset gives exactly the
-    corresponding rows of the full matrix.
+    corresponding rows of the full matrix.  ``block_mask`` ([ceil(N_q / block), ceil(N_k /
+    block)], nonzero = kept) masks every entry of a zero block.
     """
     q = _f64(q)
     k = _f64(k)
     n_q, n_k = q.shape[0], k.shape[0]
     rows = np.arange(n_q) if rows is None else np.asarray(rows, dtype=np.int64)
     s = float(scale) * (q[rows] @ k.T)
-    keys = np.arange(n_k)
-    masked = np.zeros(s.shape, dtype=bool)
-    if causal:
-        masked |= keys[None, :] > rows[:, None]
-    if kv_len is not None:
-        masked |= keys[None, :] >= int(kv_len)
-    s[masked] = -np.inf
+    s[_mask(rows, np.arange(n_k), causal, kv_len, block_mask, block)] = -np.inf
     return s
 
 
@@ -96,7 +113,8 @@ def probabilities(s, lse):
     return p
 
 
-def row_statistics(q, k, v, do, scale, causal=False, kv_len=None, rows=None):
+def row_statistics(q, k, v, do, scale, causal=False, kv_len=None, rows=None, block_mask=None,
+                   block=128):
     """Everything that is local to a set of query rows.
 
     Returns a dict with, for the selected rows:
@@ -108,7 +126,7 @@ def row_statistics(q, k, v, do, scale, causal=False, kv_len=None, rows=None):
     """
     v = _f64(v)
     rows_idx = np.arange(_f64(q).shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
-    s = masked_scores(q, k, scale, causal, kv_len, rows_idx)
+    s = masked_scores(q, k, scale, causal, kv_len, rows_idx, block_mask, block)
     lse = row_logsumexp(s)
     p = probabilities(s, lse)
     out = {"O": p @ v, "LSE": lse}
@@ -124,7 +142,7 @@ def row_statistics(q, k, v, do, scale, causal=False, kv_len=None, rows=None):
 
 
 def key_gradients(q, k, v, do, scale, lse, d_row, causal=False, kv_len=None, cols=None,
-                  rows=None):
+                  rows=None, block_mask=None, block=128):
     """dK[cols], dV[cols] as sums over the query rows ``rows`` (default: all rows).
 
     dV_j = sum_i P_ij dO_i,  dK_j = scale * sum_i dS_ij Q_i,  with P_ij = exp(s_ij - LSE_i) and
@@ -143,28 +161,25 @@ def key_gradients(q, k, v, do, scale, lse, d_row, causal=False, kv_len=None, col
     do = do[rows]
     # scores of the summed query rows against the selected keys, masked like masked_scores
     s = float(scale) * (q @ k[cols].T)
-    masked = np.zeros(s.shape, dtype=bool)
-    if causal:
-        masked |= cols[None, :] > rows[:, None]
-    if kv_len is not None:
-        masked |= cols[None, :] >= int(kv_len)
-    s[masked] = -np.inf
+    s[_mask(rows, cols, causal, kv_len, block_mask, block)] = -np.inf
     p = probabilities(s, _f64(lse))
     dp = do @ v[cols].T
     ds = p * (dp - _f64(d_row)[:, None])
     return {"dK": float(scale) * (ds.T @ q), "dV": p.T @ do}
 
 
-def attention_forward(q, k, v, scale, causal=False, kv_len=None, rows=None):
+def attention_forward(q, k, v, scale, causal=False, kv_len=None, rows=None, block_mask=None,
+                      block=128):
     """(O[rows], LSE[rows]) of exact attention for one (batch, head) slice."""
-    st = row_statistics(q, k, v, None, scale, causal, kv_len, rows)
+    st = row_statistics(q, k, v, None, scale, causal, kv_len, rows, block_mask, block)
     return st["O"], st["LSE"]
 
 
-def attention_backward(q, k, v, do, scale, causal=False, kv_len=None):
+def attention_backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, block=128):
     """Full forward + backward of one (batch, head) slice: dict with O, LSE, D, dQ, dK, dV."""
-    st = row_statistics(q, k, v, do, scale, causal, kv_len)
-    kg = key_gradients(q, k, v, do, scale, st["LSE"], st["D"], causal, kv_len)
+    st = row_statistics(q, k, v, do, scale, causal, kv_len, None, block_mask, block)
+    kg = key_gradients(q, k, v, do, scale, st["LSE"], st["D"], causal, kv_len, None, None,
+                       block_mask, block)
     st.update(kg)
     return st
 

@@ -24,26 +24,37 @@ TOL_ZERO_GRAD = 1e-4  # absolute, where the exact gradient is identically zero
 ROW_CHUNK = 2048
 
 
-def run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd=True, deterministic=False):
-    """fa_fwd (+ fa_bwd, or fa_bwd_deterministic) on cuda:0; returns device tensors."""
+def run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd=True, deterministic=False,
+            block_mask=None):
+    """fa_fwd (+ fa_bwd, or fa_bwd_deterministic) on cuda:0; returns device tensors.  With a
+    block mask (uint8 [T, T] or [H, T, T]) the block-sparse entry points run instead."""
     import exact_io_aware_fwd_gb300 as fa
 
     dev = torch.device("cuda:0")
     qd, kd, vd = (t.to(dev) for t in (q, k, v))
     kv = kv_lens.to(dev) if kv_lens is not None else None
-    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=scale, kv_lens=kv)
+    if block_mask is not None:
+        index = fa.fa_block_index_build(block_mask.to(dev), q.shape[2])
+        o, lse = fa.fa_fwd_block_sparse(qd, kd, vd, index, causal=causal, scale=scale, kv_lens=kv)
+    else:
+        o, lse = fa.fa_fwd(qd, kd, vd, causal=causal, scale=scale, kv_lens=kv)
     out = {"O": o, "LSE": lse}
     if with_bwd:
         dod = do.to(dev)
-        bwd = fa.fa_bwd_deterministic if deterministic else fa.fa_bwd
-        dq, dk, dv = bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, kv_lens=kv)
+        if block_mask is not None:
+            dq, dk, dv = fa.fa_bwd_block_sparse(qd, kd, vd, o, dod, lse, index, causal=causal,
+                                                scale=scale, kv_lens=kv,
+                                                deterministic=deterministic)
+        else:
+            bwd = fa.fa_bwd_deterministic if deterministic else fa.fa_bwd
+            dq, dk, dv = bwd(qd, kd, vd, o, dod, lse, causal=causal, scale=scale, kv_lens=kv)
         out.update(dQ=dq, dK=dk, dV=dv)
     st = fa.fa_get_error()
     assert st == fa.FA_OK, fa.fa_status_string(st)
     return out
 
 
-def oracle_slice(q, k, v, do, causal, scale, kv_len, with_bwd=True):
+def oracle_slice(q, k, v, do, causal, scale, kv_len, with_bwd=True, block_mask=None):
     """Full fp64 oracle outputs of one [N, d] slice, computed in row / key chunks."""
     q, k, v = (np.asarray(x, dtype=np.float64) for x in (q, k, v))
     do = np.asarray(do, dtype=np.float64) if with_bwd else None
@@ -51,13 +62,14 @@ def oracle_slice(q, k, v, do, causal, scale, kv_len, with_bwd=True):
     parts = []
     for r0 in range(0, n, ROW_CHUNK):
         rows = np.arange(r0, min(n, r0 + ROW_CHUNK))
-        parts.append(oracle.row_statistics(q, k, v, do, scale, causal, kv_len, rows))
+        parts.append(oracle.row_statistics(q, k, v, do, scale, causal, kv_len, rows, block_mask))
     res = {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
     if with_bwd:
         dk, dv = [], []
         for c0 in range(0, n, ROW_CHUNK):
             cols = np.arange(c0, min(n, c0 + ROW_CHUNK))
-            kg = oracle.key_gradients(q, k, v, do, scale, res["LSE"], res["D"], causal, kv_len, cols)
+            kg = oracle.key_gradients(q, k, v, do, scale, res["LSE"], res["D"], causal, kv_len, cols,
+                                      None, block_mask)
             dk.append(kg["dK"])
             dv.append(kg["dV"])
         res["dK"] = np.concatenate(dk)
@@ -112,11 +124,11 @@ def compare_slice(gpu_slice: dict, ref: dict, label: str, with_bwd=True, grad_to
 
 
 def check_case(q, k, v, do, causal, scale, kv_lens, slices=None, with_bwd=True, label="",
-               grad_tol=None, deterministic=False):
+               grad_tol=None, deterministic=False, block_mask=None):
     """Run the CUDA path on the whole batch and compare the chosen (b, h) slices."""
     B, H, N, d = q.shape
     sc = (1.0 / d ** 0.5) if scale is None else scale
-    out = run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd, deterministic)
+    out = run_gpu(q, k, v, do, causal, scale, kv_lens, with_bwd, deterministic, block_mask)
     torch.cuda.synchronize()
     slices = slices if slices is not None else [(b, h) for b in range(B) for h in range(H)]
     all_errs = []
@@ -124,7 +136,16 @@ def check_case(q, k, v, do, causal, scale, kv_lens, slices=None, with_bwd=True, 
         kv_len = int(kv_lens[b]) if kv_lens is not None else None
         ref = oracle_slice(q[b, h].float().numpy(), k[b, h].float().numpy(), v[b, h].float().numpy(),
                            do[b, h].float().numpy() if with_bwd else None, causal, sc, kv_len,
-                           with_bwd)
+                           with_bwd, _head_mask(block_mask, h))
         got = {name: f64(t[b, h]) for name, t in out.items()}
         all_errs.append(compare_slice(got, ref, f"{label} b={b} h={h}", with_bwd, grad_tol))
     return out, all_errs
+
+
+def _head_mask(block_mask, h):
+    """The [T, T] numpy block mask of head h (None without a mask)."""
+    if block_mask is None:
+        return None
+    m = block_mask.cpu().numpy()
+    return m if m.ndim == 2 else m[h]
+

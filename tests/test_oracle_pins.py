@@ -267,3 +267,102 @@ def test_key_gradients_sum_over_row_partition():
         dk += kg["dK"]
         dv += kg["dV"]
     assert np.max(np.abs(dk - st["dK"])) < 1e-13 and np.max(np.abs(dv - st["dV"])) < 1e-13
+
+
+# ---------------------------------------------------------------- block mask (block-sparse)
+
+
+def _expand(bm, block, n):
+    """Element mask of a block mask, written independently of the oracle (Kronecker product)."""
+    return np.kron(np.asarray(bm, dtype=np.int64), np.ones((block, block), dtype=np.int64))[:n, :n] != 0
+
+
+@pytest.mark.parametrize("causal,kv_len", [(False, None), (True, None), (False, 14), (True, 15)])
+def test_block_mask_against_torch_cpu_attention_float64(causal, kv_len):
+    n, d, scale, block = 19, 8, 0.4, 4
+    q, k, v, do = (_rand(n, d, s, 1.5) for s in (61, 62, 63, 64))
+    rng = np.random.default_rng(65)
+    nb = -(-n // block)
+    bm = (rng.random((nb, nb)) < 0.5).astype(np.uint8)
+    np.fill_diagonal(bm, 1)  # every row keeps at least its diagonal block
+    bm[:, 0] = 1             # ... and key block 0, so that kv_len never empties a row
+    st = oracle.attention_backward(q, k, v, do, scale, causal, kv_len, block_mask=bm, block=block)
+    mask = torch.tensor(_expand(bm, block, n))
+    if causal:
+        mask &= torch.tril(torch.ones(n, n, dtype=torch.bool))
+    if kv_len is not None:
+        mask[:, kv_len:] = False
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq[None, None], tk[None, None], tv[None, None], attn_mask=mask, scale=scale)[0, 0]
+    o.backward(torch.tensor(do))
+    assert np.max(np.abs(o.detach().numpy() - st["O"])) < 1e-12
+    for name, t in (("dQ", tq), ("dK", tk), ("dV", tv)):
+        assert np.max(np.abs(t.grad.numpy() - st[name])) < 1e-11, name
+
+
+def test_block_diagonal_mask_is_independent_attention_per_block():
+    n, d, scale, block = 12, 3, 0.8, 4
+    q, k, v, do = (_rand(n, d, s) for s in (66, 67, 68, 69))
+    bm = np.eye(3, dtype=np.uint8)
+    st = oracle.attention_backward(q, k, v, do, scale, block_mask=bm, block=block)
+    for b0 in range(0, n, block):
+        sl = slice(b0, b0 + block)
+        ref = oracle.attention_backward(q[sl], k[sl], v[sl], do[sl], scale)
+        for name in ("O", "LSE", "dQ", "dK", "dV"):
+            assert np.max(np.abs(st[name][sl] - ref[name])) < 1e-13, name
+
+
+def test_zero_block_equals_removed_keys():
+    n, d, scale, block = 9, 4, 0.6, 3
+    q, k, v, do = (_rand(n, d, s) for s in (70, 71, 72, 73))
+    bm = np.ones((3, 3), dtype=np.uint8)
+    bm[1, 2] = 0  # query rows 3..5 do not see keys 6..8
+    o, lse = oracle.attention_forward(q, k, v, scale, block_mask=bm, block=block)
+    keep = np.r_[0:6]
+    o_ref, lse_ref = oracle.attention_forward(q[3:6], k[keep], v[keep], scale)
+    assert np.max(np.abs(o[3:6] - o_ref)) < 1e-13 and np.max(np.abs(lse[3:6] - lse_ref)) < 1e-13
+    o_full, _ = oracle.attention_forward(q, k, v, scale)
+    rows = np.r_[0:3, 6:9]
+    assert np.array_equal(o[rows], o_full[rows])  # other rows keep every key: unchanged
+
+
+def test_all_ones_block_mask_is_dense_and_empty_row_is_zero():
+    n, d, scale, block = 10, 4, 0.5, 4
+    q, k, v, do = (_rand(n, d, s) for s in (74, 75, 76, 77))
+    dense = oracle.attention_backward(q, k, v, do, scale, True, 9)
+    ones = oracle.attention_backward(q, k, v, do, scale, True, 9, block_mask=np.ones((3, 3)), block=block)
+    for name in ("O", "LSE", "dQ", "dK", "dV"):
+        assert np.array_equal(dense[name], ones[name]), name
+    bm = np.ones((3, 3), dtype=np.uint8)
+    bm[1, :] = 0  # rows 4..7 keep no block
+    st = oracle.attention_backward(q, k, v, do, scale, block_mask=bm, block=block)
+    assert np.all(st["O"][4:8] == 0) and np.all(st["LSE"][4:8] == -np.inf)
+    assert np.all(st["dQ"][4:8] == 0)
+    # the other rows' gradients are those of attention without rows 4..7
+    rows = np.r_[0:4, 8:10]
+    ref = oracle.attention_backward(q[rows], k, v, do[rows], scale)
+    assert np.max(np.abs(st["dK"] - ref["dK"])) < 1e-13 and np.max(np.abs(st["dV"] - ref["dV"])) < 1e-13
+
+
+@pytest.mark.parametrize("causal,kv_len", [(False, None), (True, 5)])
+def test_block_mask_gradients_match_finite_differences(causal, kv_len):
+    n, d, scale, h, block = 6, 3, 0.7, 1e-6, 2
+    q, k, v, do = (_rand(n, d, s) for s in (78, 79, 80, 81))
+    bm = np.array([[1, 0, 1], [1, 1, 0], [0, 1, 1]], dtype=np.uint8)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention_forward(qq, kk, vv, scale, causal, kv_len, block_mask=bm, block=block)
+        return float((o * do).sum())
+
+    st = oracle.attention_backward(q, k, v, do, scale, causal, kv_len, block_mask=bm, block=block)
+    for name, x in (("dQ", q), ("dK", k), ("dV", v)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            pick = {"dQ": lambda y: (y, k, v), "dK": lambda y: (q, y, v), "dV": lambda y: (q, k, y)}[name]
+            num[idx] = (loss(*pick(xp)) - loss(*pick(xm))) / (2 * h)
+        err = np.linalg.norm(num - st[name]) / max(np.linalg.norm(num), 1e-30)
+        assert err < 1e-7, (name, err)
