@@ -200,11 +200,16 @@ def oracle_row_block(q, k, v, do, causal, scale, kv_len, rows, block_mask=None):
 
 
 def cpu_sample_inputs(w, q, k, v, do, kv):
-    b, h = 0, 0
-    f = lambda t: t[b, h].float().numpy().astype(np.float64)  # noqa: E731
-    kv_len = int(kv[b]) if kv is not None else None
-    rows_n = min(w.N, 2048)
-    rows = np.arange(w.N - rows_n, w.N)  # the last rows: the most keys under a causal mask
+    """Head 0 of batch 0 (variable-length: of the first sequence; kv is then cu_seqlens)."""
+    if w.seqlen_range is not None:
+        s0, s1 = int(kv[0]), int(kv[1])
+        f = lambda t: t[s0:s1, 0].float().numpy().astype(np.float64)  # noqa: E731
+        n, kv_len = s1 - s0, None
+    else:
+        f = lambda t: t[0, 0].float().numpy().astype(np.float64)  # noqa: E731
+        n, kv_len = w.N, (int(kv[0]) if kv is not None else None)
+    rows_n = min(n, 2048)
+    rows = np.arange(n - rows_n, n)  # the last rows: the most keys under a causal mask
     return f(q), f(k), f(v), f(do), kv_len, rows
 
 
@@ -260,26 +265,51 @@ def run_ours(args, w, world, rank, local):
     fa.load_library()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    q, k, v, do, kv = workload_inputs(w)
+    varlen = w.seqlen_range is not None
+    q, k, v, do, extra = workload_inputs(w)  # extra: kv_lens, or cu_seqlens when varlen
+    kv = None if varlen else extra
     B, H, N, d = w.B, w.H, w.N, w.d
     stream = torch.cuda.current_stream()
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     kvd = kv.to(dev) if kv is not None else None
+    cud = extra.to(dev) if varlen else None
     o = torch.empty_like(qd)
-    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    lse_shape = (H, q.shape[0]) if varlen else (B, H, N)
+    lse = torch.empty(lse_shape, device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    ws = fa.workspace_for(qd)
+    if varlen:
+        ws = torch.empty(fa.fa_bwd_varlen_workspace_size(B, q.shape[0], H, d), dtype=torch.uint8,
+                         device=dev)
+    else:
+        ws = fa.workspace_for(qd)
     f_fwd, f_bwd = w.flops()
 
     det = args.bwd == "deterministic"
     mask = workload_block_mask(w)
     index = fa.fa_block_index_build(mask.to(dev), N) if mask is not None else None
-    two_stage = det or index is not None
+    gqa = w.Hkv is not None and not varlen
+    two_stage = det or index is not None or varlen or gqa
     stages = ["fwd", "bwd"] if two_stage else ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
 
-    def step_two(evs=None):  # fa_fwd[_block_sparse], then one backward call
+    def step_two(evs=None):  # the forward call, then one backward call
         if evs is not None:
             evs[0].record(stream)
+        if varlen:
+            fa.fa_fwd_varlen(qd, kd, vd, cud, N, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            if evs is not None:
+                evs[1].record(stream)
+            fa.fa_bwd_varlen(qd, kd, vd, o, dod, lse, cud, N, causal=w.causal, scale=w.scale,
+                             deterministic=det, dq=dq, dk=dk, dv=dv, workspace=ws)
+        elif gqa:
+            fa.fa_fwd_gqa(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse)
+            if evs is not None:
+                evs[1].record(stream)
+            fa.fa_bwd_gqa(qd, kd, vd, o, dod, lse, causal=w.causal, scale=w.scale,
+                          deterministic=det, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if varlen or gqa:
+            if evs is not None:
+                evs[2].record(stream)
+            return
         if index is not None:
             fa.fa_fwd_block_sparse(qd, kd, vd, index, causal=w.causal, scale=w.scale,
                                    kv_lens=kvd, out=o, lse=lse)
@@ -350,7 +380,36 @@ def run_ours(args, w, world, rank, local):
     # ---- end to end through the public API with host buffers: pinned host inputs in, pinned
     # host outputs (O, LSE, dQ, dK, dV) out, copies overlapped with compute over head chunks
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and (varlen or gqa):
+        # host buffers in and out around the same two calls, on one stream (no chunking)
+        hin = [t.pin_memory() for t in (q, k, v, do)]
+        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+        h2d = sum(t.numel() * t.element_size() for t in hin)
+        d2h = sum(t.numel() * t.element_size() for t in hout)
+
+        def e2e_step():
+            for dst, src in zip((qd, kd, vd, dod), hin):
+                dst.copy_(src, non_blocking=True)
+            step_two()
+            for dst, src in zip(hout, (o, lse, dq, dk, dv)):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, bv = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        bv.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(bv), world) / args.steps
+        e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "chunks": 1}
+        assert fa.fa_get_error() == fa.FA_OK
+    elif not args.no_e2e:
         from exact_io_aware_fwd_gb300.pipeline import HostAttention
 
         ha = HostAttention(B, H, N, d, device=dev)
@@ -391,8 +450,9 @@ def run_ours(args, w, world, rank, local):
     dom_flops = f_fwd if dom == "fwd" else f_bwd
     achieved = dom_flops / (stage_ms[dom] * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel",
-                   "bwd": "bwd_dkdv_kernel+bwd_dq_kernel" if det else "fa_bwd_block_sparse"}[dom]
+    bwd_call = ("fa_bwd_varlen" if varlen else "fa_bwd_gqa" if gqa else
+                "fa_bwd_block_sparse" if index is not None else "fa_bwd_deterministic")
+    kernel_name = {"fwd": "fwd_kernel", "bwd_dkdv": "bwd_dkdv_kernel", "bwd": bwd_call}[dom]
     roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"bf16_tflops (burst) of {src}",
@@ -416,7 +476,8 @@ def run_ours(args, w, world, rank, local):
                    "l2": "inputs larger than L2 (no flush)" if 4 * q.numel() * 2 > 129e6 else
                    "inputs smaller than L2 (not flushed)",
                    "parallelism": f"replicas x{world}", "bwd": args.bwd,
-                   "block_mask": w.block_mask},
+                   "block_mask": w.block_mask, "Hkv": w.kv_heads,
+                   "seqlens": extra.diff().tolist() if varlen else None},
         "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,

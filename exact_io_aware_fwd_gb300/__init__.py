@@ -23,11 +23,16 @@ from .binding import (  # noqa: F401
     fa_bwd_deterministic,
     fa_bwd_dkdv,
     fa_bwd_dq_convert,
+    fa_bwd_gqa,
+    fa_bwd_varlen,
+    fa_bwd_varlen_workspace_size,
     fa_bwd_noalloc,
     fa_bwd_preprocess,
     fa_bwd_workspace_size,
     fa_fwd,
     fa_fwd_block_sparse,
+    fa_fwd_gqa,
+    fa_fwd_varlen,
     fa_get_error,
     fa_status_string,
     load_library,

@@ -32,6 +32,11 @@ EXPORTED = [
     "fa_bwd_dq_convert",
     "fa_bwd_noalloc",
     "fa_bwd_deterministic",
+    "fa_fwd_gqa",
+    "fa_bwd_gqa",
+    "fa_fwd_varlen",
+    "fa_bwd_varlen_workspace_size",
+    "fa_bwd_varlen",
     "fa_block_index_size",
     "fa_block_index_build",
     "fa_fwd_block_sparse",
@@ -76,6 +81,18 @@ def load_library(path: str | None = None):
     lib.fa_bwd_deterministic.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f,
                                           vp, vp, sz, vp]
     lib.fa_bwd_deterministic.restype = i
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, vp]
+    lib.fa_fwd_gqa.restype = i
+    lib.fa_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, i,
+                               vp, sz, vp]
+    lib.fa_bwd_gqa.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_varlen_workspace_size.restype = sz
+    lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
+                                  i, vp, sz, vp]
+    lib.fa_bwd_varlen.restype = i
     lib.fa_block_index_size.argtypes = [i, i]
     lib.fa_block_index_size.restype = sz
     lib.fa_block_index_build.argtypes = [vp, i, i, vp, sz, vp]
@@ -311,5 +328,96 @@ def fa_bwd_block_sparse(q, k, v, o, do, lse, index: BlockIndex, causal=False, sc
                                             int(bool(deterministic)), _ptr(ws), ws.numel(),
                                             _stream(stream))
     _check(st, "fa_bwd_block_sparse")
+    return dq, dk, dv
+
+
+def _check_group(q, k):
+    """(B, H, Hkv, N, d) of [B, H, N, d] queries and [B, Hkv, N, d] keys."""
+    for t in (q, k):
+        if t.dim() != 4 or not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous CUDA bfloat16 [B, heads, N, d] tensors")
+    B, H, N, d = q.shape
+    if k.shape[0] != B or k.shape[2:] != (N, d) or H % k.shape[1] != 0:
+        raise ValueError("K must be [B, Hkv, N, d] with H % Hkv == 0")
+    return B, H, k.shape[1], N, d
+
+
+def fa_fwd_gqa(q, k, v, causal=False, scale=None, kv_lens=None, out=None, lse=None, stream=None):
+    """Grouped-query forward: q [B, H, N, d], k and v [B, Hkv, N, d] (see include/fa.h)."""
+    B, H, Hkv, N, d = _check_group(q, k)
+    if v.shape != k.shape:
+        raise ValueError("V must have K's shape")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N,
+                                   d, int(bool(causal)), _scale(scale), _ptr(kv), _stream(stream))
+    _check(st, "fa_fwd_gqa")
+    return out, lse
+
+
+def fa_bwd_gqa(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, deterministic=False,
+               dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Grouped-query backward; dK, dV [B, Hkv, N, d] sum over each key/value head's group."""
+    B, H, Hkv, N, d = _check_group(q, k)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = workspace_for(q) if workspace is None else workspace
+    kv = _kv(kv_lens, B, q.device)
+    st = load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
+                                   int(bool(causal)), _scale(scale), _ptr(kv),
+                                   int(bool(deterministic)), _ptr(ws), ws.numel(),
+                                   _stream(stream))
+    _check(st, "fa_bwd_gqa")
+    return dq, dk, dv
+
+
+def _check_packed(q, k, cu_seqlens):
+    for t in (q, k):
+        if t.dim() != 3 or not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous CUDA bfloat16 [total, heads, d] tensors")
+    total, H, d = q.shape
+    if k.shape[0] != total or k.shape[2] != d or H % k.shape[1] != 0:
+        raise ValueError("K must be [total, Hkv, d] with H % Hkv == 0")
+    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+        raise ValueError("cu_seqlens must be a CUDA int32 vector of B + 1 offsets")
+    return total, H, k.shape[1], d, cu_seqlens.numel() - 1
+
+
+def fa_bwd_varlen_workspace_size(B, total, H, d) -> int:
+    return int(load_library().fa_bwd_varlen_workspace_size(int(B), int(total), int(H), int(d)))
+
+
+def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out=None, lse=None,
+                  stream=None):
+    """Packed variable-length forward: q [total, H, d], k and v [total, Hkv, d], LSE [H, total]."""
+    total, H, Hkv, d, B = _check_packed(q, k, cu_seqlens)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                      _ptr(cu_seqlens), B, int(max_seqlen), total, H, Hkv, d,
+                                      int(bool(causal)), _scale(scale), _stream(stream))
+    _check(st, "fa_fwd_varlen")
+    return out, lse
+
+
+def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, causal=False, scale=None,
+                  deterministic=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Packed variable-length backward (see include/fa.h)."""
+    total, H, Hkv, d, B = _check_packed(q, k, cu_seqlens)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        workspace = torch.empty(max(fa_bwd_varlen_workspace_size(B, total, H, d), 1),
+                                dtype=torch.uint8, device=q.device)
+    st = load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B,
+                                      int(max_seqlen), total, H, Hkv, d, int(bool(causal)),
+                                      _scale(scale), int(bool(deterministic)), _ptr(workspace),
+                                      workspace.numel(), _stream(stream))
+    _check(st, "fa_bwd_varlen")
     return dq, dk, dv
 

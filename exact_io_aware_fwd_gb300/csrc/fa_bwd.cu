@@ -66,28 +66,67 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
   }
 }
 
+// Row geometry of the preprocess and dQ-conversion kernels.  Dense: block (i, bh) is query tile i
+// of head slice bh of [B*H, N, d].  Variable-length: block (i, b*H + h) is tile i of sequence b,
+// head h of the packed [total, H, d] tensors, whose workspace tile is h * ws_tiles + tile0 + i.
+struct RowGeo {
+  const int32_t* cu;  // token offsets [B + 1] (variable-length only)
+  int H, total, ws_tiles;
+};
+
+template <bool kVarlen>
+struct TileRows {
+  int n;                // rows of this sequence (dense: N)
+  size_t ws_tile;       // workspace tile (stats rows ws_tile * 128 + r, dQ accumulator tile)
+  size_t tok0;          // dense: bh * N; variable-length: first token of the sequence
+  int heads, h;         // variable-length: row stride in heads and this head
+  __device__ TileRows(int i, int bh, int N, int nqt, const RowGeo& g) {
+    if constexpr (kVarlen) {
+      const int b = bh / g.H;
+      h = bh - b * g.H;
+      heads = g.H;
+      int start;
+      seq_bounds(g.cu, b, g.total, start, n);
+      tok0 = static_cast<size_t>(start);
+      ws_tile = static_cast<size_t>(h) * g.ws_tiles + seq_tile0(start, b) + i;
+    } else {
+      n = N;
+      h = 0;
+      heads = 1;
+      tok0 = static_cast<size_t>(bh) * N;
+      ws_tile = static_cast<size_t>(bh) * nqt + i;
+    }
+  }
+  __device__ size_t row(int q) const {  // element offset / D of row q ([.., d] rows)
+    return kVarlen ? (tok0 + q) * heads + h : tok0 + q;
+  }
+  __device__ size_t lse(int q, int total) const {  // LSE index of row q
+    return kVarlen ? static_cast<size_t>(h) * total + tok0 + q : tok0 + q;
+  }
+};
+
 // ------------------------------------------------------------------------------------------
-// Preprocess: grid (num_qtiles, BH), 256 threads.
-template <int D>
+// Preprocess: grid (query tiles, B*H), 256 threads.
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
                                                              const __nv_bfloat16* __restrict__ dO,
                                                              const float* __restrict__ lse, int N,
                                                              int nqt, float* __restrict__ neg_lse2,
                                                              float* __restrict__ neg_delta,
                                                              float* __restrict__ dq_acc,
-                                                             int zero_acc) {
+                                                             int zero_acc, RowGeo geo) {
   constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
   constexpr int RPW = 32 / G;  // rows per warp per pass
   const int i = blockIdx.x;
-  const int bh = blockIdx.y;
-  const int npad = nqt * 128;
+  const TileRows<kVarlen> tr(i, blockIdx.y, N, nqt, geo);
+  if (kVarlen && i * 128 >= tr.n) return;  // past this sequence's end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / G, cl = lane % G;
   for (int rr = warp * RPW + sub; rr < 128; rr += 8 * RPW) {
     const int q = i * 128 + rr;
     float acc = 0.f;
-    if (q < N) {
-      const size_t off = (static_cast<size_t>(bh) * N + q) * D + cl * 8;
+    if (q < tr.n) {
+      const size_t off = tr.row(q) * D + cl * 8;
       const uint4 o = __ldg(reinterpret_cast<const uint4*>(O + off));
       const uint4 g = __ldg(reinterpret_cast<const uint4*>(dO + off));
       const uint32_t ov[4] = {o.x, o.y, o.z, o.w}, gv[4] = {g.x, g.y, g.z, g.w};
@@ -98,33 +137,34 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 #pragma unroll
     for (int m = G / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (cl == 0) {
-      const size_t idx = static_cast<size_t>(bh) * npad + q;
+      const size_t idx = tr.ws_tile * 128 + rr;
       float l2 = INFINITY;
-      if (q < N) {
-        const float l = __ldg(lse + static_cast<size_t>(bh) * N + q);
+      if (q < tr.n) {
+        const float l = __ldg(lse + tr.lse(q, geo.total));
         l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;  // a row with no key: P must be 0
       }
       neg_lse2[idx] = -l2;
-      neg_delta[idx] = (q < N) ? -acc : 0.f;
+      neg_delta[idx] = (q < tr.n) ? -acc : 0.f;
     }
   }
   if (!zero_acc) return;
-  float4* t = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D);
+  float4* t = reinterpret_cast<float4*>(dq_acc + tr.ws_tile * 128 * D);
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int idx = threadIdx.x; idx < 32 * D; idx += 256) t[idx] = z;
 }
 
 // ------------------------------------------------------------------------------------------
-// dQ convert: grid (num_qtiles, BH), 256 threads; thread = (row r, pair of column groups).
-template <int D>
+// dQ convert: grid (query tiles, B*H), 256 threads; thread = (row r, pair of column groups).
+template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
                                                              __nv_bfloat16* __restrict__ dQ, int N,
-                                                             int nqt, float scale) {
-  const int i = blockIdx.x, bh = blockIdx.y;
+                                                             int nqt, float scale, RowGeo geo) {
+  const int i = blockIdx.x;
+  const TileRows<kVarlen> tr(i, blockIdx.y, N, nqt, geo);
   const int r = threadIdx.x & 127;
   const int q = i * 128 + r;
-  if (q >= N) return;
-  const float* tile = acc + (static_cast<size_t>(bh) * nqt + i) * 128 * D;
+  if (q >= tr.n) return;
+  const float* tile = acc + tr.ws_tile * 128 * D;
   for (int cp = threadIdx.x >> 7; cp < D / 8; cp += 2) {
     const float4 a0 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp) * 128 + r) * 4));
     const float4 a1 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp + 1) * 128 + r) * 4));
@@ -133,7 +173,7 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
     o.y = pack_bf16(a0.z * scale, a0.w * scale);
     o.z = pack_bf16(a1.x * scale, a1.y * scale);
     o.w = pack_bf16(a1.z * scale, a1.w * scale);
-    *reinterpret_cast<uint4*>(dQ + (static_cast<size_t>(bh) * N + q) * D + cp * 8) = o;
+    *reinterpret_cast<uint4*>(dQ + tr.row(q) * D + cp * 8) = o;
   }
 }
 
@@ -187,7 +227,10 @@ constexpr int kBwdThreads = 128 * (1 + kGroups);
 // GEMM, no drain, no atomics, no dS copy in shared memory).
 // kSparse: block-sparse; the key tile visits only the query tiles its mask column keeps (a
 // descending list from the block index, whose prefix of tiles >= the key tile is the causal part).
-template <int D, bool kWithDQ, bool kSparse>
+// kVarlen: packed variable-length batch (see the forward kernel); grouped-query attention (Hkv <
+// H) makes the CTA of key/value head hk walk the query tiles of all H / Hkv heads of its group,
+// so dK and dV sum over the group in tensor memory.
+template <int D, bool kWithDQ, bool kSparse, bool kVarlen>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -226,24 +269,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // ---- work item: head-major (one or two heads' Q, dO and dQ accumulator live in L2 at a
   // time); within a head key tile 0 first (with a causal mask the lowest tiles have most work)
   const int lin = blockIdx.x;
-  const int bh = lin / a.num_qtiles;
+  const int bkv = lin / a.num_qtiles;  // (b, key/value head)
   const int j = lin % a.num_qtiles;
-  const int b = bh / a.H;
-  const int N = a.N;
-  const int nqt = a.num_qtiles;
-  const int npad = nqt * 128;
+  const int b = bkv / a.Hkv;
+  const int hk = bkv - b * a.Hkv;
+  const int G = a.H / a.Hkv;  // query heads per key/value head
+  int seq_start = 0, N = a.N;
+  if constexpr (kVarlen) seq_bounds(a.cu_seqlens, b, a.total, seq_start, N);
+  if (kVarlen && j * 128 >= N) return;  // past this sequence's end (uniform over the CTA)
+  const int nqt = kVarlen ? (N + 127) / 128 : a.num_qtiles;  // this sequence's query tiles
   int kv_len = N;
-  if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  if (!kVarlen && a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
   const int i0 = a.causal ? j : 0;
-  int nI = (j * 128 < kv_len) ? (nqt - i0) : 0;  // query tiles this key tile visits
+  int nI = (j * 128 < kv_len) ? (nqt - i0) : 0;  // query tiles this key tile visits per head
+  // workspace rows / dQ accumulator tiles of query head h: (ws_head(h) * ws_tiles + tile0 + i)
+  const int ws_tile0 = kVarlen ? seq_tile0(seq_start, b) : 0;
+  auto ws_head = [&](int h) { return kVarlen ? h : b * a.H + h; };
+  // TMA box coordinates (y, z) of row r: dense (r, head slice), packed (head, token)
+  auto q_y = [&](int h, int r) { return kVarlen ? h : r; };
+  auto q_z = [&](int h, int r) { return kVarlen ? seq_start + r : b * a.H + h; };
+  const int kv_y = kVarlen ? hk : j * 128;
+  const int kv_z = kVarlen ? seq_start + j * 128 : bkv;
   const int32_t* c_list = nullptr;
   if constexpr (kSparse) {
     const BlockIndex BI = block_index_layout(nqt);
-    const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bh % a.H) * BI.words);
+    // (block-sparse calls have Hkv == H: bkv is the query head slice)
+    const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bkv % a.H) * BI.words);
     c_list = base + BI.cidx + static_cast<int64_t>(j) * nqt;
     nI = (j * 128 < kv_len) ? __ldg(base + (a.causal ? BI.cccnt : BI.ccnt) + j) : 0;
   }
   auto qtile = [&](int it) { return kSparse ? __ldg(c_list + it) : i0 + it; };
+  // iteration it -> (query head of the group, query tile); G == 1 without grouped queries
+  auto head_of = [&](int it) { return hk * G + (G == 1 ? 0 : it / nI); };
+  auto tile_of = [&](int it) { return qtile(G == 1 ? it : it % nI); };
+  const int nIt = nI * G;  // iterations of the CTA
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
@@ -274,29 +333,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ================= TMA producer
-    if (lane == 0 && nI > 0) {
+    if (lane == 0 && nIt > 0) {
       mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sm + L::kK + c * 16384, &tmK, kv_full, c * 64, j * 128, bh);
-        tma_load_3d(sm + L::kV + c * 16384, &tmV, kv_full, c * 64, j * 128, bh);
+        tma_load_3d(sm + L::kK + c * 16384, &tmK, kv_full, c * 64, kv_y, kv_z);
+        tma_load_3d(sm + L::kV + c * 16384, &tmV, kv_full, c * 64, kv_y, kv_z);
       }
       int nq = 0, ndo = 0;
-      for (int it = 0; it < nI; ++it) {
-        const int i = qtile(it), s = it & 1;
+      for (int it = 0; it < nIt; ++it) {
+        const int h = head_of(it), i = tile_of(it), s = it & 1;
         const uint32_t ph = (it >> 1) & 1;
         if (!mbar_wait(&q_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&q_full[s], L::kTile + 1024);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kQ + s * L::kTile + c * 16384, &tmQ, &q_full[s], c * 64, i * 128, bh);
-        const size_t srow = static_cast<size_t>(bh) * npad + i * 128;
+          tma_load_3d(sm + L::kQ + s * L::kTile + c * 16384, &tmQ, &q_full[s], c * 64,
+                      q_y(h, i * 128), q_z(h, i * 128));
+        const size_t srow =
+            (static_cast<size_t>(ws_head(h)) * a.ws_tiles + ws_tile0 + i) * 128;
         bulk_load(sm + L::kLse + s * 512, a.neg_lse2 + srow, 512, &q_full[s]);
         bulk_load(sm + L::kDelta + s * 512, a.neg_delta + srow, 512, &q_full[s]);
         nq = it + 1;
         if (!mbar_wait(&do_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&do_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kDO + s * L::kTile + c * 16384, &tmdO, &do_full[s], c * 64, i * 128,
-                      bh);
+          tma_load_3d(sm + L::kDO + s * L::kTile + c * 16384, &tmdO, &do_full[s], c * 64,
+                      q_y(h, i * 128), q_z(h, i * 128));
         ndo = it + 1;
       }
       if (*abort_flag) {
@@ -308,7 +369,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ================= MMA issuer
-    if (lane == 0 && nI > 0) {
+    if (lane == 0 && nIt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major operands
       constexpr uint32_t idKV = idesc_bf16(128, D, false, true);    // dV, dK: A in TMEM, B MN-major
       constexpr uint32_t idQ = idesc_bf16(128, D, true, true);      // dQ: A = dS MN-major, B MN-major
@@ -382,23 +443,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_dV(0);
-        if (nI > 1 && (ok = wait_q(1))) {
+        if (nIt > 1 && (ok = wait_q(1))) {
           tc_fence_after();
           issue_S(1);
         }
       }
-      for (int it = 0; ok && it < nI; ++it) {
+      for (int it = 0; ok && it < nIt; ++it) {
         if (!(ok = mbar_wait(ds_full, it & 1, ctl))) break;
         tc_fence_after();
         issue_dK_dQ(it);
-        if (it + 1 < nI) {
+        if (it + 1 < nIt) {
           if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl))) break;
           tc_fence_after();
           issue_dV(it + 1);
           if (!(ok = wait_do(it + 1) && (!kWithDQ || mbar_wait(dq_empty, it & 1, ctl)))) break;
           tc_fence_after();
           issue_dP(it + 1);
-          if (it + 2 < nI) {
+          if (it + 2 < nIt) {
             if (!(ok = wait_q(it + 2))) break;
             tc_fence_after();
             issue_S(it + 2);
@@ -427,10 +488,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     // dQ_i (query row r of the tile, this group's columns) into the fp32 accumulator: load,
     // release the tensor memory (dP_{i+1} waits for it), then the atomics, which overlap dP_{i+1}
-    auto drain = [&](int it, int qt) -> bool {  // qt: query tile of iteration it
+    auto drain = [&](int it, int qh, int qt) -> bool {  // (qh, qt): query head, tile of it
       if (!mbar_wait_warp(dq_full, it & 1, ctl)) return false;
       tc_fence_after();
-      float* tile = a.dq_acc + (static_cast<size_t>(bh) * nqt + qt) * 128 * D;
+      float* tile =
+          a.dq_acc + (static_cast<size_t>(ws_head(qh)) * a.ws_tiles + ws_tile0 + qt) * 128 * D;
       const int g0 = (kDC / 4) * grp;  // first 4-column group of this group's columns
       uint32_t va[32], vb[32];
       if (kDC >= 32) tmem_ld32(tDQ, va);
@@ -458,9 +520,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     };
 
     bool ok = true;
-    int i_prev = 0;  // query tile of the previous iteration (its dQ is drained in this one)
-    for (int it = 0; it < nI; ++it) {
-      const int i = qtile(it), s = it & 1;
+    int h_prev = 0, i_prev = 0;  // previous iteration's query head and tile (drained in this one)
+    for (int it = 0; it < nIt; ++it) {
+      const int h = head_of(it), i = tile_of(it), s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
       if (!(ok = mbar_wait_warp(&q_full[s], ph, ctl))) break;  // LSE and D are in smem
       if (!(ok = mbar_wait_warp(s_full, it & 1, ctl))) break;
@@ -502,7 +564,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
 
-      if (kWithDQ && it > 0 && !(ok = drain(it - 1, i_prev))) break;
+      if (kWithDQ && it > 0 && !(ok = drain(it - 1, h_prev, i_prev))) break;
 
       if (!(ok = mbar_wait_warp(dp_full, it & 1, ctl))) break;
       tc_fence_after();
@@ -543,16 +605,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
+      h_prev = h;
       i_prev = i;
     }
-    if (kWithDQ && ok && nI > 0) ok = drain(nI - 1, i_prev);
+    if (kWithDQ && ok && nIt > 0) ok = drain(nIt - 1, h_prev, i_prev);
 
     // ---- epilogue: the 64-column panels of dV and scale * dK (bf16, swizzled, over the V or K
     // tile in smem, which no MMA reads any more) are shared out over the groups; one TMA store
     // per panel
-    if (ok && nI > 0) ok = mbar_wait_warp(dkdv_full, 0, ctl);
+    if (ok && nIt > 0) ok = mbar_wait_warp(dkdv_full, 0, ctl);
     constexpr int kPanels = 2 * (D / 64);  // dV panels, then dK panels
-    if (ok && nI > 0) tc_fence_after();
+    if (ok && nIt > 0) tc_fence_after();
+    // variable-length: a key tile that runs past its sequence's end is stored row by row
+    const bool direct = kVarlen && (j * 128 + 128 > N);
     for (int pn = grp; pn < kPanels; pn += kGroups) {
       const bool is_dk = pn >= D / 64;
       const int cp = pn % (D / 64);  // column panel within the matrix
@@ -563,7 +628,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t v[32];
-          if (nI > 0) {
+          if (nIt > 0) {
             tmem_ld32(tmem + lanes + col + 32 * c, v);
             tmem_wait_ld();
             reg_fence(v);
@@ -575,17 +640,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * mul, __uint_as_float(v[2 * e + 1]) * mul);
+          if (direct) {
+            if (key < N) {
+              uint4* dst = reinterpret_cast<uint4*>(
+                  static_cast<__nv_bfloat16*>(is_dk ? a.dk : a.dv) +
+                  (static_cast<size_t>(seq_start + key) * a.Hkv + hk) * D + 64 * cp + 32 * c);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            st_shared_v4(panel + sw128_offset(r, 4 * c + g), pk[4 * g], pk[4 * g + 1],
-                         pk[4 * g + 2], pk[4 * g + 3]);
+              for (int g = 0; g < 4; ++g)
+                dst[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              st_shared_v4(panel + sw128_offset(r, 4 * c + g), pk[4 * g], pk[4 * g + 1],
+                           pk[4 * g + 2], pk[4 * g + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(1 + grp, 128);  // every warp of the group arrives, aborted or not
-      if (quad == 0 && lane == 0 && !*abort_flag) {
+      if (!direct && quad == 0 && lane == 0 && !*abort_flag) {
         tma_store_3d(is_dk ? &tmdK : &tmdV, sm + (is_dk ? L::kK : L::kV) + cp * 16384, cp * 64,
-                     j * 128, bh);
+                     kv_y, kv_z);
         bulk_commit();
         bulk_wait_read0();
       }
@@ -609,12 +685,32 @@ cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const fl
   const dim3 grid(nqt, BH);
   auto o = static_cast<const __nv_bfloat16*>(O);
   auto g = static_cast<const __nv_bfloat16*>(dO);
+  const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc,
-                                                    zero_acc ? 1 : 0);
+    bwd_preprocess_kernel<64, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta,
+                                                           dq_acc, zero_acc ? 1 : 0, geo);
   else
-    bwd_preprocess_kernel<128><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta, dq_acc,
-                                                     zero_acc ? 1 : 0);
+    bwd_preprocess_kernel<128, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2,
+                                                            neg_delta, dq_acc, zero_acc ? 1 : 0,
+                                                            geo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, const float* lse,
+                                         const int32_t* cu, int B, int H, int max_tiles,
+                                         int total, int ws_tiles, float* neg_lse2,
+                                         float* neg_delta, float* dq_acc, bool zero_acc,
+                                         cudaStream_t s) {
+  const dim3 grid(max_tiles, B * H);
+  auto o = static_cast<const __nv_bfloat16*>(O);
+  auto g = static_cast<const __nv_bfloat16*>(dO);
+  const RowGeo geo{cu, H, total, ws_tiles};
+  if (d == 64)
+    bwd_preprocess_kernel<64, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
+                                                          dq_acc, zero_acc ? 1 : 0, geo);
+  else
+    bwd_preprocess_kernel<128, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
+                                                           dq_acc, zero_acc ? 1 : 0, geo);
   return cudaGetLastError();
 }
 
@@ -623,29 +719,45 @@ cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, 
   const int nqt = (N + 127) / 128;
   const dim3 grid(nqt, BH);
   auto out = static_cast<__nv_bfloat16*>(dQ);
+  const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
-    bwd_dq_convert_kernel<64><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale);
+    bwd_dq_convert_kernel<64, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, geo);
   else
-    bwd_dq_convert_kernel<128><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale);
+    bwd_dq_convert_kernel<128, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, geo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, void* dQ, const int32_t* cu,
+                                         int B, int H, int max_tiles, int total, int ws_tiles,
+                                         float scale, cudaStream_t s) {
+  const dim3 grid(max_tiles, B * H);
+  auto out = static_cast<__nv_bfloat16*>(dQ);
+  const RowGeo geo{cu, H, total, ws_tiles};
+  if (d == 64)
+    bwd_dq_convert_kernel<64, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, geo);
+  else
+    bwd_dq_convert_kernel<128, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, geo);
   return cudaGetLastError();
 }
 
 namespace {
-template <int D, bool kWithDQ, bool kSparse>
+template <int D, bool kWithDQ, bool kSparse, bool kVarlen>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv,
                           BwdArgs a, cudaStream_t st) {
   using L = BwdLayout<D>;
   constexpr uint32_t kMaxSmem = 232448;  // 227 KB, the per-block opt-in limit of sm_100-family GPUs
   const uint32_t smem = (L::kBytes + 1024 <= kMaxSmem) ? L::kBytes + 1024 : kMaxSmem;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ, kSparse>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ, kSparse, kVarlen>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
-  const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dkdv_kernel<D, kWithDQ, kSparse><<<grid, kBwdThreads, smem, st>>>(tq, tk, tv, tdo, tdk,
-                                                                        tdv, a);
+  // one CTA per (b, key/value head, key tile)
+  const unsigned grid = static_cast<unsigned>(a.num_qtiles) *
+                        static_cast<unsigned>(a.BH / a.H * a.Hkv);
+  bwd_dkdv_kernel<D, kWithDQ, kSparse, kVarlen><<<grid, kBwdThreads, smem, st>>>(
+      tq, tk, tv, tdo, tdk, tdv, a);
   return cudaGetLastError();
 }
 }  // namespace
@@ -653,18 +765,18 @@ cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
 cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdk,
                             const CUtensorMap& tdv, const BwdArgs& a, cudaStream_t s) {
-  if (a.blk != nullptr) {
-    if (d == 64)
-      return with_dq ? launch_dkdv_d<64, true, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                     : launch_dkdv_d<64, false, true>(tq, tk, tv, tdo, tdk, tdv, a, s);
-    return with_dq ? launch_dkdv_d<128, true, true>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                   : launch_dkdv_d<128, false, true>(tq, tk, tv, tdo, tdk, tdv, a, s);
+#define FA_DKDV(DD, WQ, SP, VL) launch_dkdv_d<DD, WQ, SP, VL>(tq, tk, tv, tdo, tdk, tdv, a, s)
+  if (a.cu_seqlens != nullptr) {  // variable-length (not combined with a block mask)
+    if (d == 64) return with_dq ? FA_DKDV(64, true, false, true) : FA_DKDV(64, false, false, true);
+    return with_dq ? FA_DKDV(128, true, false, true) : FA_DKDV(128, false, false, true);
   }
-  if (d == 64)
-    return with_dq ? launch_dkdv_d<64, true, false>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                   : launch_dkdv_d<64, false, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
-  return with_dq ? launch_dkdv_d<128, true, false>(tq, tk, tv, tdo, tdk, tdv, a, s)
-                 : launch_dkdv_d<128, false, false>(tq, tk, tv, tdo, tdk, tdv, a, s);
+  if (a.blk != nullptr) {
+    if (d == 64) return with_dq ? FA_DKDV(64, true, true, false) : FA_DKDV(64, false, true, false);
+    return with_dq ? FA_DKDV(128, true, true, false) : FA_DKDV(128, false, true, false);
+  }
+  if (d == 64) return with_dq ? FA_DKDV(64, true, false, false) : FA_DKDV(64, false, false, false);
+  return with_dq ? FA_DKDV(128, true, false, false) : FA_DKDV(128, false, false, false);
+#undef FA_DKDV
 }
 
 }  // namespace fa

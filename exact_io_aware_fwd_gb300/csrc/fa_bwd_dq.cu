@@ -72,7 +72,7 @@ __device__ __forceinline__ int warp_count_below_dq(const int32_t* list, int cnt,
   return total;
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -106,17 +106,29 @@ __global__ void __launch_bounds__(384, 1)
   }
 
   // ---- work item: query tile i of (b, h); causal: the tiles with most key tiles first
-  const int nqt = a.num_qtiles;
+  const int nqt_grid = a.num_qtiles;
   const int lin = blockIdx.x;
   const int bh = lin % a.BH;
-  const int i = a.causal ? (nqt - 1 - lin / a.BH) : (lin / a.BH);
+  const int i = a.causal ? (nqt_grid - 1 - lin / a.BH) : (lin / a.BH);
   const int b = bh / a.H;
-  const int N = a.N;
-  const int npad = nqt * 128;
+  const int h = bh - b * a.H;
+  const int hk = h / (a.H / a.Hkv);
+  int seq_start = 0, N = a.N;
+  if constexpr (kVarlen) seq_bounds(a.cu_seqlens, b, a.total, seq_start, N);
+  if (kVarlen && i * 128 >= N) return;  // past this sequence's end (uniform over the CTA)
+  const int nqt = kVarlen ? (N + 127) / 128 : nqt_grid;
   int kv_len = N;
-  if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  if (!kVarlen && a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
   int nkeys = kv_len;
   if (a.causal) nkeys = min(nkeys, i * 128 + 128);
+  // TMA box coordinates (y, z): dense (row, head slice), packed (head, token)
+  const int q_y = kVarlen ? h : i * 128, q_z = kVarlen ? seq_start + i * 128 : bh;
+  auto kv_y = [&](int kt) { return kVarlen ? hk : kt * 128; };
+  auto kv_z = [&](int kt) { return kVarlen ? seq_start + kt * 128 : b * a.Hkv + hk; };
+  // workspace row of query row qi
+  const size_t ws_row0 =
+      (kVarlen ? (static_cast<size_t>(h) * a.ws_tiles + seq_tile0(seq_start, b) + i)
+               : (static_cast<size_t>(bh) * a.ws_tiles + i)) * 128;
   const int nb_dense = (nkeys + 127) / 128;  // key tiles 0 .. nb_dense-1 are visible
   const int32_t* r_list = nullptr;
   int* cnt_smem = reinterpret_cast<int*>(sm + L::kCnt);
@@ -160,8 +172,8 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0 && nb > 0) {
       mbar_arrive_expect_tx(qdo_full, 2 * L::kTile);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sm + L::kQ + c * 16384, &tmQ, qdo_full, c * 64, i * 128, bh);
-        tma_load_3d(sm + L::kDO + c * 16384, &tmdO, qdo_full, c * 64, i * 128, bh);
+        tma_load_3d(sm + L::kQ + c * 16384, &tmQ, qdo_full, c * 64, q_y, q_z);
+        tma_load_3d(sm + L::kDO + c * 16384, &tmdO, qdo_full, c * 64, q_y, q_z);
       }
       int nk = 0, nv = 0;
       for (int jj = 0; jj < nb; ++jj) {
@@ -171,12 +183,14 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&k_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, kt * 128, bh);
+          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, kv_y(kt),
+                      kv_z(kt));
         nk = jj + 1;
         if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&v_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, kt * 128, bh);
+          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, kv_y(kt),
+                      kv_z(kt));
         nv = jj + 1;
       }
       if (*abort_flag) {
@@ -261,7 +275,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lanes = (quad * 32u) << 16;
     const uint32_t tS = tmem + lanes + L::kColS + 64 * grp;
     const float c2 = a.scale_log2;
-    const size_t srow = static_cast<size_t>(bh) * npad + qi;  // < npad: always in the workspace
+    const size_t srow = ws_row0 + r;  // padded rows of the tile hold -inf / 0
     const float nl2 = a.neg_lse2[srow];   // -LSE * log2(e) (-inf on padded rows: P = 0)
     const float ndl = a.neg_delta[srow];  // -D
     const float2 cc = make_float2(c2, c2);
@@ -329,6 +343,8 @@ __global__ void __launch_bounds__(384, 1)
     // clipped).  d = 128: one 64-column panel per group; d = 64: the first group alone.
     if (ok && nb > 0) ok = mbar_wait_warp(dq_full, 0, ctl);
     const bool writer = (D == 128) || grp == 0;
+    // variable-length: a tile that runs past its sequence's end is stored row by row
+    const bool direct = kVarlen && (i * 128 + 128 > N);
     if (writer) {
       const int c0 = (D == 128) ? 64 * grp : 0;  // first dQ column of this group
       if (ok) {
@@ -348,17 +364,28 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(__uint_as_float(v[2 * e]) * a.scale, __uint_as_float(v[2 * e + 1]) * a.scale);
-          const uint32_t panel = sbase + L::kQ + (c0 / 64) * 16384;
+          if (direct) {
+            if (qi < N) {
+              uint4* dst = reinterpret_cast<uint4*>(
+                  static_cast<__nv_bfloat16*>(a.dq) +
+                  (static_cast<size_t>(seq_start + qi) * a.H + h) * D + c0 + 32 * c);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            st_shared_v4(panel + sw128_offset(r, 4 * c + g), pk[4 * g], pk[4 * g + 1],
-                         pk[4 * g + 2], pk[4 * g + 3]);
+              for (int g = 0; g < 4; ++g)
+                dst[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+          } else {
+            const uint32_t panel = sbase + L::kQ + (c0 / 64) * 16384;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              st_shared_v4(panel + sw128_offset(r, 4 * c + g), pk[4 * g], pk[4 * g + 1],
+                           pk[4 * g + 2], pk[4 * g + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(1 + grp, 128);  // every warp of the group arrives, aborted or not
-      if (quad == 0 && lane == 0 && !*abort_flag) {
-        tma_store_3d(&tmdQ, sm + L::kQ + (c0 / 64) * 16384, c0, i * 128, bh);
+      if (!direct && quad == 0 && lane == 0 && !*abort_flag) {
+        tma_store_3d(&tmdQ, sm + L::kQ + (c0 / 64) * 16384, c0, q_y, q_z);
         bulk_commit();
         bulk_wait_read0();
       }
@@ -373,7 +400,7 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kVarlen>
 cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, BwdArgs a,
                         cudaStream_t st) {
@@ -382,13 +409,13 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // tcgen05.alloc: ask for enough shared memory (d = 64 needs less than half an SM's) that one
   // CTA fills the SM.
   const uint32_t smem = L::kBytes + 1024 < 120u * 1024u ? 120u * 1024u : L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, kSparse>,
+  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, kSparse, kVarlen>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);
-  bwd_dq_kernel<D, kSparse><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdq, a);
+  bwd_dq_kernel<D, kSparse, kVarlen><<<grid, 384, smem, st>>>(tq, tk, tv, tdo, tdq, a);
   return cudaGetLastError();
 }
 
@@ -397,12 +424,16 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
                           const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                           const BwdArgs& a, cudaStream_t s) {
-  if (a.blk != nullptr) {
-    if (d == 64) return launch_dq_d<64, true>(tq, tk, tv, tdo, tdq, a, s);
-    return launch_dq_d<128, true>(tq, tk, tv, tdo, tdq, a, s);
+  if (a.cu_seqlens != nullptr) {
+    if (d == 64) return launch_dq_d<64, false, true>(tq, tk, tv, tdo, tdq, a, s);
+    return launch_dq_d<128, false, true>(tq, tk, tv, tdo, tdq, a, s);
   }
-  if (d == 64) return launch_dq_d<64, false>(tq, tk, tv, tdo, tdq, a, s);
-  return launch_dq_d<128, false>(tq, tk, tv, tdo, tdq, a, s);
+  if (a.blk != nullptr) {
+    if (d == 64) return launch_dq_d<64, true, false>(tq, tk, tv, tdo, tdq, a, s);
+    return launch_dq_d<128, true, false>(tq, tk, tv, tdo, tdq, a, s);
+  }
+  if (d == 64) return launch_dq_d<64, false, false>(tq, tk, tv, tdo, tdq, a, s);
+  return launch_dq_d<128, false, false>(tq, tk, tv, tdo, tdq, a, s);
 }
 
 }  // namespace fa

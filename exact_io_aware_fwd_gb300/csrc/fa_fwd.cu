@@ -24,6 +24,11 @@
 //    (page two, FlashAttention-1 section, causal paragraph).
 //  * epilogue: O~ / l -> bf16 -> swizzled smem (over the Q tile) -> TMA store (rows >= N are
 //    clipped by the tensor map); LSE with plain coalesced stores.
+//  * variable-length (kVarlen): packed [total, H, d] tensors with per-sequence token offsets;
+//    a sequence's tiles are 3-D TMA boxes (d, head, token) that may run into the next
+//    sequence: those keys are masked like padding, and the rows of a sequence's last tile are
+//    stored one by one instead of by the (sequence-blind) TMA store.  Grouped-query attention
+//    reads K and V of head h / (H / Hkv).
 //  * block-sparse (kSparse): the K/V stream is the union of the kept key tiles of the CTA's two
 //    query tiles (a sorted list from the block index); each query tile runs S, softmax and P V
 //    only on its own kept tiles, so skipped tiles cost neither loads nor MMAs (page two,
@@ -97,7 +102,7 @@ __device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, in
   return total;
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -134,18 +139,34 @@ __global__ void __launch_bounds__(384, 1)
   // group block level major (all heads of one level together) and, with a causal mask, the
   // heaviest blocks first, so that every wave holds CTAs of similar length and the light ones
   // fill the tail.  Groups run one after another.
+  // (variable-length: block level major over every (b, h), heaviest first when causal)
   const int lin = blockIdx.x;
-  const int gsz = a.head_group * a.num_qblocks;  // CTAs per full group
-  const int grp = lin / gsz;
-  const int heads = min(a.head_group, a.BH - grp * a.head_group);  // heads in this group
-  const int idx = lin - grp * gsz;
-  const int bh = grp * a.head_group + idx % heads;
-  const int qb = a.causal ? (a.num_qblocks - 1 - idx / heads) : (idx / heads);
+  int bh, qb;
+  if constexpr (kVarlen) {
+    bh = lin % a.BH;
+    qb = a.causal ? (a.num_qblocks - 1 - lin / a.BH) : (lin / a.BH);
+  } else {
+    const int gsz = a.head_group * a.num_qblocks;  // CTAs per full group
+    const int grp = lin / gsz;
+    const int heads = min(a.head_group, a.BH - grp * a.head_group);  // heads in this group
+    const int idx = lin - grp * gsz;
+    bh = grp * a.head_group + idx % heads;
+    qb = a.causal ? (a.num_qblocks - 1 - idx / heads) : (idx / heads);
+  }
   const int b = bh / a.H;
-  const int N = a.N;
-  int kv_len = N;
-  if (a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  const int h = bh - b * a.H;
+  const int hk = h / (a.H / a.Hkv);  // key/value head
+  int seq_start = 0, N = a.N;        // this sequence's first token and length
+  if constexpr (kVarlen) seq_bounds(a.cu_seqlens, b, a.total, seq_start, N);
   const int q0 = qb * 256;
+  if (kVarlen && q0 >= N) return;  // past this sequence's end (uniform over the CTA)
+  int kv_len = N;
+  if (!kVarlen && a.kv_lens != nullptr) kv_len = min(max(__ldg(a.kv_lens + b), 0), N);
+  // TMA box coordinates (y, z) of row r: dense (r, head slice), packed (head, token)
+  const int q_y0 = kVarlen ? h : 0, q_z0 = kVarlen ? seq_start : bh;
+  const int kv_y0 = kVarlen ? hk : 0, kv_z0 = kVarlen ? seq_start : b * a.Hkv + hk;
+  auto row_y = [&](int y0, int r) { return kVarlen ? y0 : r; };
+  auto row_z = [&](int z0, int r) { return kVarlen ? z0 + r : z0; };
   int nb[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
@@ -226,8 +247,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive_expect_tx(q_full, ntiles * L::kTile);
       for (int t = 0; t < ntiles; ++t)
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64, q0 + 128 * t,
-                      bh);
+          tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64,
+                      row_y(q_y0, q0 + 128 * t), row_z(q_z0, q0 + 128 * t));
       int jk = 0, jv = 0;  // K and V tiles whose copies have been issued
       for (int j = 0; j < npos; ++j) {
         const int s = j % S;
@@ -236,14 +257,14 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&k_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64, kt * 128,
-                      bh);
+          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64,
+                      row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
         jk = j + 1;
         if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
         mbar_arrive_expect_tx(&v_full[s], L::kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64, kt * 128,
-                      bh);
+          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64,
+                      row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
         jv = j + 1;
       }
       if (*abort_flag) {
@@ -446,6 +467,9 @@ __global__ void __launch_bounds__(384, 1)
 
     // ---- epilogue: O = O~ / l -> bf16 -> swizzled smem over Q_t -> TMA store; LSE
     const bool tile_live = (qt0 < N);
+    // variable-length: a tile that runs past its sequence's end would have the TMA store write
+    // into the next sequence, so its rows are stored one by one
+    const bool direct = kVarlen && (qt0 + 128 > N);
     if (ok && n > 0) ok = mbar_wait_warp(&o_full[t], 0, ctl);
     // block-sparse: a tile with no kept key tile still had its Q copied in (for the other tile's
     // sake); that copy must land before the staging below reuses its shared memory
@@ -472,23 +496,37 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 16; ++e)
             pk[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv_l,
                               __uint_as_float(o[2 * e + 1]) * inv_l);
-          const uint32_t panel = stage + ((32 * c) / 64) * 16384;
-          const uint32_t g0 = ((32 * c) % 64) / 8;
+          if (direct) {
+            if (qi < N) {
+              uint4* dst = reinterpret_cast<uint4*>(
+                  static_cast<__nv_bfloat16*>(a.o) +
+                  (static_cast<size_t>(seq_start + qi) * a.H + h) * D + 32 * c);
 #pragma unroll
-          for (int g = 0; g < 4; ++g)
-            st_shared_v4(panel + sw128_offset(row, g0 + g), pk[4 * g], pk[4 * g + 1],
-                         pk[4 * g + 2], pk[4 * g + 3]);
+              for (int g = 0; g < 4; ++g)
+                dst[g] = make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+            }
+          } else {
+            const uint32_t panel = stage + ((32 * c) / 64) * 16384;
+            const uint32_t g0 = ((32 * c) % 64) / 8;
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              st_shared_v4(panel + sw128_offset(row, g0 + g), pk[4 * g], pk[4 * g + 1],
+                           pk[4 * g + 2], pk[4 * g + 3]);
+          }
         }
         if (qi < N) {
           const float lse = (l_run > 0.f) ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
-          a.lse[static_cast<size_t>(bh) * N + qi] = lse;
+          const size_t at = kVarlen ? static_cast<size_t>(h) * a.total + seq_start + qi
+                                    : static_cast<size_t>(bh) * N + qi;
+          a.lse[at] = lse;
         }
       }
       fence_proxy_async_smem();
       named_bar_sync(1 + t, 128);  // every warp of the group arrives, aborted or not
-      if (quad == 0 && lane == 0 && !*abort_flag) {
+      if (!direct && quad == 0 && lane == 0 && !*abort_flag) {
         for (int c = 0; c < D / 64; ++c)
-          tma_store_3d(&tmO, sm + L::kQ + t * L::kTile + c * 16384, c * 64, qt0, bh);
+          tma_store_3d(&tmO, sm + L::kQ + t * L::kTile + c * 16384, c * 64, row_y(q_y0, qt0),
+                       row_z(q_z0, qt0));
         bulk_commit();
         bulk_wait_read0();
       }
@@ -503,18 +541,18 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kVarlen>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, FwdArgs a, cudaStream_t st) {
   using L = FwdLayout<D>;
   const uint32_t smem = L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kSparse>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kSparse, kVarlen>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qblocks) * static_cast<unsigned>(a.BH);
-  fwd_kernel<D, kSparse><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
+  fwd_kernel<D, kSparse, kVarlen><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -522,12 +560,16 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t s) {
-  if (a.blk != nullptr) {
-    if (d == 64) return launch_fwd_d<64, true>(tq, tk, tv, to, a, s);
-    return launch_fwd_d<128, true>(tq, tk, tv, to, a, s);
+  if (a.cu_seqlens != nullptr) {  // variable-length (not combined with a block mask)
+    if (d == 64) return launch_fwd_d<64, false, true>(tq, tk, tv, to, a, s);
+    return launch_fwd_d<128, false, true>(tq, tk, tv, to, a, s);
   }
-  if (d == 64) return launch_fwd_d<64, false>(tq, tk, tv, to, a, s);
-  return launch_fwd_d<128, false>(tq, tk, tv, to, a, s);
+  if (a.blk != nullptr) {
+    if (d == 64) return launch_fwd_d<64, true, false>(tq, tk, tv, to, a, s);
+    return launch_fwd_d<128, true, false>(tq, tk, tv, to, a, s);
+  }
+  if (d == 64) return launch_fwd_d<64, false, false>(tq, tk, tv, to, a, s);
+  return launch_fwd_d<128, false, false>(tq, tk, tv, to, a, s);
 }
 
 }  // namespace fa

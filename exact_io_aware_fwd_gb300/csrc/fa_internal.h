@@ -35,15 +35,35 @@ __host__ __device__ inline BlockIndex block_index_layout(int T) {
   return L;
 }
 
+// Rows of one sequence in the packed variable-length layout [total, heads, d]: sequence b holds
+// tokens [cu[b], cu[b+1]) (clamped to [0, total], so any offsets stay in bounds).
+__host__ __device__ inline void seq_bounds(const int32_t* cu, int b, int total, int& start,
+                                           int& len) {
+  int s0 = cu[b], s1 = cu[b + 1];
+  s0 = s0 < 0 ? 0 : (s0 > total ? total : s0);
+  s1 = s1 < s0 ? s0 : (s1 > total ? total : s1);
+  start = s0;
+  len = s1 - s0;
+}
+// First 128-row tile of sequence b in the per-head variable-length workspace: ceil(start / 128)
+// + b never overlaps sequence b - 1's tiles and stays below ceil(total / 128) + B.
+__host__ __device__ inline int seq_tile0(int start, int b) { return (start + 127) / 128 + b; }
+
 // Forward kernel arguments (tensor maps travel separately as __grid_constant__ parameters).
+// Dense layout: [B, H, N, d] (K, V: [B, Hkv, N, d]).  Variable-length layout (cu_seqlens set):
+// packed [total, H, d] (K, V: [total, Hkv, d]), N is the longest sequence.
 struct FwdArgs {
   int H, N, BH;
+  int Hkv;                // key/value heads: H, or a divisor of H (grouped-query attention)
   int num_qblocks;        // 256-row query blocks per (b, h)
   int head_group;         // heads scheduled together (their K/V stay resident in L2)
   int causal;
   float scale_log2;       // scale * log2(e)
   const int32_t* kv_lens; // device int32[B] or nullptr
-  float* lse;             // [B, H, N] fp32
+  float* lse;             // [B, H, N] fp32 (variable-length: [H, total])
+  void* o;                // O itself (variable-length: rows of a sequence's last tile)
+  const int32_t* cu_seqlens;  // variable-length token offsets [B + 1], or nullptr
+  int total;              // variable-length: tokens in the packed tensors
   const int32_t* blk;     // block-sparse index (BlockIndex layout) or nullptr for dense
   int blk_heads;          // mask heads in blk: 1 (shared by every head) or H
   int* status;            // library status word (device)
@@ -53,7 +73,15 @@ struct FwdArgs {
 
 struct BwdArgs {
   int H, N, BH;
+  int Hkv;                // key/value heads (grouped-query attention when < H)
   int num_qtiles;         // ceil(N / 128) = padded rows / 128
+  int ws_tiles;           // 128-row tiles per head in the workspace: num_qtiles (dense), or
+                          // ceil(total / 128) + B (variable-length, see seq_tile0)
+  const int32_t* cu_seqlens;  // variable-length token offsets [B + 1], or nullptr
+  int total;
+  void* dq;               // dQ, dK, dV themselves (variable-length: rows of a last tile)
+  void* dk;
+  void* dv;
   int causal;
   float scale;            // softmax scale (dK is scaled by it at the end)
   float scale_log2;       // scale * log2(e)
@@ -68,7 +96,8 @@ struct BwdArgs {
   uint32_t smem_bytes;
 };
 
-// Workspace layout (all offsets 256-byte aligned): dq_acc | -LSE*log2(e) | -D
+// Workspace layout (all offsets 256-byte aligned): dq_acc | -LSE*log2(e) | -D.  BH heads of N
+// rows padded to 128; the variable-length workspace is workspace_layout(H, ws_tiles * 128, d).
 struct Workspace {
   size_t dq_acc_off, neg_lse2_off, neg_delta_off, total;
 };
@@ -80,6 +109,15 @@ cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse,
                                   int BH, int N, float* neg_lse2, float* neg_delta, float* dq_acc,
                                   bool zero_acc, cudaStream_t s);
+// variable-length preprocess / dQ conversion: grid over (tile, b, h) of a packed batch
+cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, const float* lse,
+                                         const int32_t* cu, int B, int H, int max_tiles,
+                                         int total, int ws_tiles, float* neg_lse2,
+                                         float* neg_delta, float* dq_acc, bool zero_acc,
+                                         cudaStream_t s);
+cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, void* dQ, const int32_t* cu,
+                                         int B, int H, int max_tiles, int total, int ws_tiles,
+                                         float scale, cudaStream_t s);
 // with_dq: accumulate dQ with atomics (fa_bwd); without: dK, dV only (deterministic path)
 cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,

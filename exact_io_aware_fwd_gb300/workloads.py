@@ -10,6 +10,11 @@ Recipe (one generator per workload, ``torch.Generator().manual_seed(seed)`` on t
      next from the same generator.
 Layout: contiguous [B, H, N, d] bfloat16, the order the attention signature uses.
 
+Grouped-query workloads (Hkv < H) draw K and V with Hkv heads: Q [B, H, N, d], K, V
+[B, Hkv, N, d], dO [B, H, N, d], in that order.  Variable-length workloads first draw the B
+sequence lengths ``torch.randint(lo, hi + 1, (B,))``, then Q, K, V, dO packed as [total, heads, d]
+(sequence b = tokens cu[b] .. cu[b+1]-1, cu the running sum of the lengths).
+
 Block-sparse workloads add a block mask over 128 x 128 tiles (uint8 [T, T], T = ceil(N / 128),
 nonzero = kept), shared by every batch and head.  The pages name a fixed butterfly pattern for
 the block-sparse extension without drawing it; ``butterfly_block_mask`` takes the support of the
@@ -39,7 +44,13 @@ class Workload:
     kv_len_range: tuple | None = None  # inclusive (lo, hi) of per-batch key lengths
     oracle_slices: int = 0  # (batch, head) slices the oracle checks at full size (0 = all)
     block_mask: str | None = None  # "butterfly": block-sparse over 128 x 128 tiles
+    Hkv: int | None = None  # key/value heads (grouped-query attention) when set
+    seqlen_range: tuple | None = None  # variable-length: B packed sequences, lengths U{lo..hi}
     notes: str = field(default="", compare=False)
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
 
     @property
     def scale(self) -> float:
@@ -48,6 +59,11 @@ class Workload:
     def flops(self) -> tuple[float, float]:
         """(forward, backward) FLOPs: 4 N^2 d and 10 N^2 d per head, halved when causal.  With a
         block mask N^2 becomes the area of the kept tiles (a causal diagonal tile counts half)."""
+        if self.seqlen_range is not None:  # sum of per-sequence N^2 over the packed batch
+            lens = draw_lengths(self).double()
+            per_head = float((lens * lens).sum()) * self.d
+            f, b = 4.0 * per_head * self.H, 10.0 * per_head * self.H
+            return (f / 2, b / 2) if self.causal else (f, b)
         if self.block_mask is not None:
             bm = workload_block_mask(self).bool()
             t = bm.shape[0]
@@ -85,7 +101,17 @@ SPARSE_WORKLOADS = [
              block_mask="butterfly"),
 ]
 
-BY_NAME = {w.name: w for w in WORKLOADS + SPARSE_WORKLOADS}
+# Grouped-query attention on the long-context shape (8 key/value heads for 32 query heads), and a
+# packed batch of 16 causal sequences of 512..4096 tokens (N is the longest allowed length).
+GQA_WORKLOADS = [
+    Workload("gqa-1x32kv8x16384x128", 1, 32, 16384, 128, True, seed=6, oracle_slices=2, Hkv=8),
+]
+VARLEN_WORKLOADS = [
+    Workload("varlen-16x16x512-4096x128", 16, 16, 4096, 128, True, seed=7, oracle_slices=3,
+             seqlen_range=(512, 4096)),
+]
+
+BY_NAME = {w.name: w for w in WORKLOADS + SPARSE_WORKLOADS + GQA_WORKLOADS + VARLEN_WORKLOADS}
 HEADLINE = WORKLOADS[3]
 
 
@@ -111,7 +137,39 @@ def make_inputs(B, H, N, d, seed, sigma_qk=1.0, sigma_vdo=1.0, kv_len_range=None
 
 
 def workload_inputs(w: Workload):
+    """(q, k, v, do, extra): extra is kv_lens (dense, may be None) or cu_seqlens (variable-length,
+    int32 [B + 1], tensors packed [total, heads, d])."""
+    if w.seqlen_range is not None:
+        return make_varlen_inputs(draw_lengths(w), w.H, w.kv_heads, w.d, w.seed)
+    if w.Hkv is not None:
+        return make_gqa_inputs(w.B, w.H, w.Hkv, w.N, w.d, w.seed) + (None,)
     return make_inputs(w.B, w.H, w.N, w.d, w.seed, w.sigma_qk, w.sigma_vdo, w.kv_len_range)
+
+
+def make_gqa_inputs(B, H, Hkv, N, d, seed):
+    """(q, k, v, do) with q, do [B, H, N, d] and k, v [B, Hkv, N, d], all N(0, 1) in bf16."""
+    g = torch.Generator().manual_seed(int(seed))
+    shapes = [(B, H, N, d), (B, Hkv, N, d), (B, Hkv, N, d), (B, H, N, d)]
+    return tuple(torch.randn(sh, generator=g).to(torch.bfloat16) for sh in shapes)
+
+
+def draw_lengths(w: Workload) -> torch.Tensor:
+    """The B sequence lengths of a variable-length workload (int32, from its own seed)."""
+    lo, hi = w.seqlen_range
+    g = torch.Generator().manual_seed(int(w.seed))
+    return torch.randint(lo, hi + 1, (w.B,), generator=g).to(torch.int32)
+
+
+def make_varlen_inputs(lengths, H, Hkv, d, seed):
+    """(q, k, v, do, cu_seqlens): sequences of the given lengths packed as [total, heads, d]."""
+    lengths = torch.as_tensor(lengths, dtype=torch.int32)
+    cu = torch.zeros(lengths.numel() + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lengths, 0)
+    total = int(cu[-1])
+    g = torch.Generator().manual_seed(int(seed) + 1)
+    shapes = [(total, H, d), (total, Hkv, d), (total, Hkv, d), (total, H, d)]
+    q, k, v, do = (torch.randn(sh, generator=g).to(torch.bfloat16) for sh in shapes)
+    return q, k, v, do, cu
 
 
 def sample_slices(w: Workload, count=None, seed_offset=1000):

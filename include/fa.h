@@ -118,6 +118,47 @@ fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, cons
                                void* stream);
 
 /*
+ * Grouped-query attention (multi-query when Hkv == 1): H query heads share Hkv key/value heads,
+ * query head h reading K and V of head h / (H / Hkv).  Q, O, dO, dQ: [B, H, N, d]; K, V, dK,
+ * dV: [B, Hkv, N, d]; LSE [B, H, N]; H % Hkv == 0.  dK and dV of a key/value head sum the
+ * gradients of all its query heads (accumulated in tensor memory, no atomics).  Otherwise the
+ * arguments, results and workspace (fa_bwd_workspace_size(B, H, N, d)) of fa_fwd / fa_bwd;
+ * deterministic != 0 as fa_bwd_deterministic.  GQA/MQA is a feature of the official library the
+ * pages list (page "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section "独立 flash-attn
+ * 与 PyTorch SDPA 的区别").
+ */
+fa_status fa_fwd_gqa(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     int B, int H, int Hkv, int N, int d, int causal, float scale,
+                     const int32_t* kv_lens, void* stream);
+fa_status fa_bwd_gqa(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                     const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int Hkv,
+                     int N, int d, int causal, float scale, const int32_t* kv_lens,
+                     int deterministic, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Variable-length (packed, un-padded) batches: B sequences of different lengths stored back to
+ * back, as the official library's varlen interface does (same section of the same page; the
+ * un-padded layout is also a headline of FlashAttention-4, section "硬件、数据类型、确定性与填充
+ * 注意事项").  Sequence b is tokens [cu_seqlens[b], cu_seqlens[b + 1]) of
+ *   Q, O, dO, dQ: [total, H, d] bf16;  K, V, dK, dV: [total, Hkv, d] bf16;  LSE: [H, total] fp32,
+ * and attends only to itself (self-attention; the causal mask is per sequence).
+ * cu_seqlens: DEVICE int32[B + 1], non-decreasing, cu_seqlens[0] = 0, cu_seqlens[B] = total
+ * (offsets are clamped to [0, total]).  max_seqlen: at least the longest sequence (sizes the
+ * grid; tokens beyond it are not computed).  H % Hkv == 0 (grouped-query as above).
+ * Workspace: fa_bwd_varlen_workspace_size(B, total, H, d) bytes, 256-byte aligned.
+ * A sequence of length 0 produces nothing; total == 0 launches nothing.
+ */
+fa_status fa_fwd_varlen(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                        const int32_t* cu_seqlens, int B, int max_seqlen, int total, int H,
+                        int Hkv, int d, int causal, float scale, void* stream);
+size_t fa_bwd_varlen_workspace_size(int B, int total, int H, int d);
+fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void* O,
+                        const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                        const int32_t* cu_seqlens, int B, int max_seqlen, int total, int H,
+                        int Hkv, int d, int causal, float scale, int deterministic,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Block-sparse attention.  A block mask over tiles of 128 queries x 128 keys keeps or drops
  * whole tiles: the scores of query i and key j count only where
  * block_mask[i / 128][j / 128] != 0 (and the causal and key-length masks keep them too); the

@@ -149,3 +149,38 @@ def _head_mask(block_mask, h):
     m = block_mask.cpu().numpy()
     return m if m.ndim == 2 else m[h]
 
+
+
+def compare_grad(g, r, label, tol=None):
+    """Relative Frobenius error of one gradient (or the zero-gradient bound), asserted."""
+    assert np.all(np.isfinite(g)), f"{label}: non-finite"
+    nrm = np.linalg.norm(r)
+    if nrm == 0:
+        err = float(np.max(np.abs(g))) if g.size else 0.0
+        assert err <= TOL_ZERO_GRAD, (label, err)
+    else:
+        err = float(np.linalg.norm(g - r) / nrm)
+        assert err <= (tol or TOL_GRAD_REL), (label, err)
+    return err
+
+
+def check_heads(q_h, k_g, v_g, do_h, out_h, causal, scale, kv_len, label, grad_tol=None):
+    """One key/value head and its group of query heads.
+
+    q_h, do_h: lists (one per query head of the group) of [n, d] CPU bf16 slices; k_g, v_g: the
+    group's [n, d] key/value slices; out_h: list of dicts of GPU results for those query heads
+    (O, LSE, dQ as CPU float64) plus "dK", "dV" of the key/value head.  The oracle runs per
+    query head; dK and dV of the shared head are the sums over the group (the chain rule for a
+    shared input)."""
+    k_np, v_np = k_g.float().numpy(), v_g.float().numpy()
+    dk_ref = dv_ref = None
+    for qq, dd, got in zip(q_h, do_h, out_h):
+        ref = oracle_slice(qq.float().numpy(), k_np, v_np, dd.float().numpy(), causal, scale,
+                           kv_len, True)
+        fwd = {"O": got["O"], "LSE": got["LSE"]}
+        compare_slice(fwd, ref, label, with_bwd=False)
+        compare_grad(got["dQ"], ref["dQ"], label + " dQ", grad_tol)
+        dk_ref = ref["dK"] if dk_ref is None else dk_ref + ref["dK"]
+        dv_ref = ref["dV"] if dv_ref is None else dv_ref + ref["dV"]
+    compare_grad(out_h[0]["dK"], dk_ref, label + " dK", grad_tol)
+    compare_grad(out_h[0]["dV"], dv_ref, label + " dV", grad_tol)
