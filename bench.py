@@ -35,11 +35,15 @@ from exact_io_aware_fwd_gb300.workloads import (BY_NAME, HEADLINE, workload_bloc
 
 METRIC = "attention fwd/bwd TFLOPS (bf16, 1\u00d7GB300) and % of dense BF16 tensor peak"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-SOURCES_FOR_TRAFFIC = ["exact_io_aware_fwd_gb300/csrc/fa_api.cu",
-                       "exact_io_aware_fwd_gb300/csrc/fa_bwd.cu",
-                       "exact_io_aware_fwd_gb300/csrc/fa_fwd.cu",
-                       "exact_io_aware_fwd_gb300/csrc/fa_internal.h",
-                       "exact_io_aware_fwd_gb300/csrc/sm103.cuh"]
+# Sources whose change invalidates a recorded DRAM-traffic figure, per kernel (the launch setup
+# in fa_api.cu and the shared headers count for every kernel).
+_COMMON = ["exact_io_aware_fwd_gb300/csrc/fa_api.cu", "exact_io_aware_fwd_gb300/csrc/fa_internal.h",
+           "exact_io_aware_fwd_gb300/csrc/sm103.cuh"]
+SOURCES_FOR_TRAFFIC = {
+    "fwd": _COMMON + ["exact_io_aware_fwd_gb300/csrc/fa_fwd.cu"],
+    "bwd": _COMMON + ["exact_io_aware_fwd_gb300/csrc/fa_bwd.cu",
+                      "exact_io_aware_fwd_gb300/csrc/fa_bwd_dq.cu"],
+}
 
 
 def parse():
@@ -52,6 +56,10 @@ def parse():
     ap.add_argument("--bwd", default="atomic", choices=["atomic", "deterministic"],
                     help="backward entry: fa_bwd (dQ by fp32 atomics) or fa_bwd_deterministic")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ingest-ncu", metavar="CSV", default=None,
+                    help="record the DRAM bytes of an ncu launch list of --workload in "
+                         "profiles/traffic.json and exit (no GPU needed)")
+    ap.add_argument("--ncu-command", default="", help="the ncu command that wrote --ingest-ncu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=None,
                     help="override H (smaller profiling captures of the same shape); the line "
@@ -101,25 +109,80 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def sources_digest():
+def sources_digest(kind):
+    """Short hash of the kernel sources of `kind` ("fwd" or "bwd")."""
     h = hashlib.sha256()
-    for rel in SOURCES_FOR_TRAFFIC:
+    for rel in SOURCES_FOR_TRAFFIC[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    """DRAM bytes per launch (per call, for a multi-kernel backward call) from the committed ncu
+    summary, if it was taken on the current sources of that kernel."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
+    if kernel.startswith("fa_bwd"):  # a backward call of several kernels: their sum per call
+        kernel = "bwd_step"
     e = d.get(f"{kernel}@{workload}")
-    if not e or e.get("sources") != sources_digest():
+    kind = "fwd" if kernel.startswith("fwd") else "bwd"
+    if not e or e.get("sources") != sources_digest(kind):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+def ingest_ncu(csv_path, workload, command):
+    """Record the DRAM bytes of an ncu launch list (``--metrics gpu__time_duration.sum,
+    dram__bytes_read.sum,dram__bytes_write.sum --csv``) of `workload` in profiles/traffic.json:
+    per kernel the mean per launch, and "bwd_step" = the sum of the backward kernels' means."""
+    import collections
+    import csv
+    import re
+
+    rows = list(csv.reader(open(csv_path)))
+    hi = next(i for i, r in enumerate(rows) if r and r[0] == "ID")
+    hdr = rows[hi]
+    col = {k: hdr.index(k) for k in ("ID", "Kernel Name", "Metric Name", "Metric Unit",
+                                     "Metric Value")}
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "nsecond": 1, "usecond": 1e3,
+             "msecond": 1e6, "ns": 1, "us": 1e3, "ms": 1e6}
+    launches = collections.defaultdict(dict)
+    names = {}
+    for r in rows[hi + 1:]:
+        v = float(r[col["Metric Value"]].replace(",", "")) * scale.get(r[col["Metric Unit"]], 1)
+        launches[r[col["ID"]]][r[col["Metric Name"]]] = v
+        names[r[col["ID"]]] = r[col["Kernel Name"]]
+    agg = collections.defaultdict(list)
+    for i, m in launches.items():
+        base = re.search(r"(\w+_kernel)", names[i]).group(1)
+        agg[base].append(m)
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    d = json.load(open(p)) if os.path.exists(p) else {}
+    d["_note"] = ("DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum, mean over "
+                  "the launches of the list) from full-size launch lists; 'command' is the ncu "
+                  "command, 'sources' the digest of the kernel's sources it ran; bench.py reports "
+                  "a figure only while the digest matches")
+    step = {"dram_bytes_per_launch": 0.0, "read": 0.0, "write": 0.0, "ns_per_launch": 0.0}
+    for base, ms in agg.items():
+        mean = lambda k: sum(m[k] for m in ms) / len(ms)  # noqa: E731
+        e = {"dram_bytes_per_launch": mean("dram__bytes_read.sum") + mean("dram__bytes_write.sum"),
+             "read": mean("dram__bytes_read.sum"), "write": mean("dram__bytes_write.sum"),
+             "ns_per_launch": mean("gpu__time_duration.sum"), "launches": len(ms),
+             "sources": sources_digest("fwd" if base.startswith("fwd") else "bwd"),
+             "command": command}
+        d[f"{base}@{workload}"] = e
+        if base.startswith("bwd_"):
+            for k in step:
+                step[k] += e[k]
+    if step["ns_per_launch"] > 0:
+        d[f"bwd_step@{workload}"] = dict(step, sources=sources_digest("bwd"), command=command)
+    with open(p, "w") as f:
+        json.dump(d, f, indent=1, sort_keys=True)
+        f.write("\n")
 
 
 class ClockSampler:
@@ -493,6 +556,9 @@ def run_ours(args, w, world, rank, local):
 
 def main():
     args = parse()
+    if args.ingest_ncu:
+        ingest_ncu(args.ingest_ncu, args.workload, args.ncu_command)
+        return
     w = BY_NAME[args.workload]
     if args.heads is not None:
         from dataclasses import replace

@@ -139,20 +139,15 @@ __global__ void __launch_bounds__(384, 1)
   // group block level major (all heads of one level together) and, with a causal mask, the
   // heaviest blocks first, so that every wave holds CTAs of similar length and the light ones
   // fill the tail.  Groups run one after another.
-  // (variable-length: block level major over every (b, h), heaviest first when causal)
+  // (variable-length: the same order with the longest sequence's block count; the blocks past a
+  // shorter sequence's end exit at once)
   const int lin = blockIdx.x;
-  int bh, qb;
-  if constexpr (kVarlen) {
-    bh = lin % a.BH;
-    qb = a.causal ? (a.num_qblocks - 1 - lin / a.BH) : (lin / a.BH);
-  } else {
-    const int gsz = a.head_group * a.num_qblocks;  // CTAs per full group
-    const int grp = lin / gsz;
-    const int heads = min(a.head_group, a.BH - grp * a.head_group);  // heads in this group
-    const int idx = lin - grp * gsz;
-    bh = grp * a.head_group + idx % heads;
-    qb = a.causal ? (a.num_qblocks - 1 - idx / heads) : (idx / heads);
-  }
+  const int gsz = a.head_group * a.num_qblocks;  // CTAs per full group
+  const int grp = lin / gsz;
+  const int heads = min(a.head_group, a.BH - grp * a.head_group);  // heads in this group
+  const int idx = lin - grp * gsz;
+  const int bh = grp * a.head_group + idx % heads;
+  const int qb = a.causal ? (a.num_qblocks - 1 - idx / heads) : (idx / heads);
   const int b = bh / a.H;
   const int h = bh - b * a.H;
   const int hk = h / (a.H / a.Hkv);  // key/value head
