@@ -387,42 +387,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto desc_do = [&](int it) {
         return sdesc_sw128(sbase + L::kDO + (it & 1) * L::kTile, 16384, 1024);
       };
-      auto kmaj = [](int kk) -> uint64_t {  // K-major k-step: 32 B inside a panel, 16 KB panels
-        return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
+      // Each product is one chain of K-steps (sm103.cuh); with two elementwise groups the
+      // packed P^T / dS^T halves sit at columns [0, 32) and [64, 96) (packed_col).
+      auto ts_chain = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t acc) {
+        if constexpr (kQG == 64) {
+          mma_ts_k128_split(d, a, b, idKV, acc);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(d, a + packed_col(kk), b + kk * 128, idKV, (acc || kk > 0) ? 1u : 0u);
+        }
       };
       auto issue_S = [&](int it) {  // S^T = K_j Q_i^T
-        const uint64_t dq = desc_q(it);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColS, desc_k + kmaj(kk), dq + kmaj(kk), idS, kk > 0 ? 1u : 0u);
+        mma_ss_kmajor<D>(tmem + L::kColS, desc_k, desc_q(it), idS, 0u);
         mma_commit(s_full);
       };
       auto issue_dP = [&](int it) {  // dP^T = V_j dO_i^T
-        const uint64_t ddo = desc_do(it);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColDP, desc_v + kmaj(kk), ddo + kmaj(kk), idS, kk > 0 ? 1u : 0u);
+        mma_ss_kmajor<D>(tmem + L::kColDP, desc_v, desc_do(it), idS, 0u);
         mma_commit(dp_full);
       };
       auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA: +2 KB rows)
-        const uint64_t ddo = desc_do(it);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + L::kColDV, tmem + L::kColS + packed_col(kk), ddo + kk * 128, idKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+        ts_chain(tmem + L::kColDV, tmem + L::kColS, desc_do(it), it > 0 ? 1u : 0u);
         mma_commit(&do_empty[it & 1]);
       };
       auto issue_dK_dQ = [&](int it) {
-        const uint64_t dq = desc_q(it);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q_i
-          mma_ts(tmem + L::kColDK, tmem + L::kColDP + packed_col(kk), dq + kk * 128, idKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+        ts_chain(tmem + L::kColDK, tmem + L::kColDP, desc_q(it), it > 0 ? 1u : 0u);  // dK += dS^T Q_i
         mma_commit(&q_empty[it & 1]);
-        if (kWithDQ) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
-            mma_ss(tmem + L::kColDP, desc_ds + kk * 128, desc_k + kk * 128, idQ, kk > 0 ? 1u : 0u);
+        if (kWithDQ) {  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
+          mma_ss_mn_k128(tmem + L::kColDP, desc_ds, desc_k, idQ, 0u);
           mma_commit(dq_full);
         }
       };

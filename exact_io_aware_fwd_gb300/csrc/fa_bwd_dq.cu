@@ -55,9 +55,6 @@ struct DqLayout {
   static constexpr uint32_t kTmemCols = 512;
 };
 
-// Packed bf16 column of the 16-key k-step kk (0..7) in a dP buffer (each group packs its dS over
-// the first half of its own 64 columns).
-__device__ __forceinline__ uint32_t dq_packed_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 // Entries of the ascending list[0, cnt) below lim (whole warp).
 __device__ __forceinline__ int warp_count_below_dq(const int32_t* list, int cnt, int lim) {
@@ -209,31 +206,18 @@ __global__ void __launch_bounds__(384, 1)
       const uint64_t desc_do = sdesc_sw128(sbase + L::kDO, 16384, 1024);
       auto desc_k = [&](int jj) { return sdesc_sw128(sbase + L::kK + (jj & 1) * L::kTile, 16384, 1024); };
       auto desc_v = [&](int jj) { return sdesc_sw128(sbase + L::kV + (jj & 1) * L::kTile, 16384, 1024); };
-      auto kmaj = [](int kk) -> uint64_t {
-        return static_cast<uint64_t>(((kk >> 2) * 16384 + (kk & 3) * 32) >> 4);
-      };
-      auto issue_S = [&](int jj) {  // S = Q_i K_j^T
-        const uint64_t dk = desc_k(jj);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColS, desc_q + kmaj(kk), dk + kmaj(kk), idS, kk > 0 ? 1u : 0u);
+      auto issue_S = [&](int jj) {  // S = Q_i K_j^T (one chain of K-steps, sm103.cuh)
+        mma_ss_kmajor<D>(tmem + L::kColS, desc_q, desc_k(jj), idS, 0u);
         mma_commit(s_full);
       };
       auto issue_dP = [&](int jj) {  // dP = dO_i V_j^T into buffer jj % 2
-        const uint64_t dv = desc_v(jj);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::kColDP + 128 * (jj & 1), desc_do + kmaj(kk), dv + kmaj(kk), idS,
-                 kk > 0 ? 1u : 0u);
+        mma_ss_kmajor<D>(tmem + L::kColDP + 128 * (jj & 1), desc_do, desc_v(jj), idS, 0u);
         mma_commit(&dp_full[jj & 1]);
         mma_commit(&v_empty[jj & 1]);
       };
-      auto issue_dQ = [&](int jj) {  // dQ += dS_j K_j  (128 keys, 16 per MMA)
-        const uint64_t dk = desc_k(jj);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + L::kColDQ, tmem + L::kColDP + 128 * (jj & 1) + dq_packed_col(kk),
-                 dk + kk * 128, idQ, (jj > 0 || kk > 0) ? 1u : 0u);
+      auto issue_dQ = [&](int jj) {  // dQ += dS_j K_j  (128 keys, 16 per MMA; dS halves split)
+        mma_ts_k128_split(tmem + L::kColDQ, tmem + L::kColDP + 128 * (jj & 1), desc_k(jj), idQ,
+                          jj > 0 ? 1u : 0u);
         mma_commit(&k_empty[jj & 1]);
       };
       auto wait_k = [&](int jj) { return mbar_wait(&k_full[jj & 1], (jj >> 1) & 1, ctl); };

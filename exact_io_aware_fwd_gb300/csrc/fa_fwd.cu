@@ -295,15 +295,10 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const uint32_t qbs0 = sbase + L::kQ;
         const uint32_t kbs = sbase + L::kK + s * L::kTile;
-        auto issue_S = [&](int t) {  // S_t = Q_t K_j^T
-          const uint32_t qbs = qbs0 + t * L::kTile;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            const uint64_t adesc = sdesc_sw128(qbs + off, 16384, 1024);
-            const uint64_t bdesc = sdesc_sw128(kbs + off, 16384, 1024);
-            mma_ss(tmem + L::kColS0 + 128 * t, adesc, bdesc, idS, kk > 0 ? 1u : 0u);
-          }
+        auto issue_S = [&](int t) {  // S_t = Q_t K_j^T, all D / 16 K-steps in one chain
+          mma_ss_kmajor<D>(tmem + L::kColS0 + 128 * t,
+                           sdesc_sw128(qbs0 + t * L::kTile, 16384, 1024),
+                           sdesc_sw128(kbs, 16384, 1024), idS, 0u);
           mma_commit(&s_full[t]);
           ++cnt[t];
         };
@@ -320,15 +315,10 @@ __global__ void __launch_bounds__(384, 1)
           if ((use_prev >> t) & 1u) {
             if (!(ok = mbar_wait(&p_full[t], (cnt[t] - 1) & 1, ctl))) break;
             tc_fence_after();
-            const uint32_t vb = sbase + L::kV + sp * L::kTile;
-            const uint32_t colS = L::kColS0 + 128 * t;
-            const uint32_t colO = L::kColO0 + D * t;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {  // 128 keys, 16 per MMA; P packed 2 per column
-              const uint64_t bdesc = sdesc_sw128(vb + kk * 2048, 16384, 1024);
-              mma_ts(tmem + colO, tmem + colS + kk * 8, bdesc, idO,
-                     (cnt[t] > 1 || kk > 0) ? 1u : 0u);
-            }
+            // O_t += P_t V: 128 keys, 16 per MMA, P packed 2 per column, V rows +2 KB per step
+            mma_ts_k128_step8(tmem + L::kColO0 + D * t, tmem + L::kColS0 + 128 * t,
+                              sdesc_sw128(sbase + L::kV + sp * L::kTile, 16384, 1024), idO,
+                              cnt[t] > 1 ? 1u : 0u);
             if (cnt[t] == ncnt[t]) mma_commit(&o_full[t]);  // the tile's last P V
           }
           // S_t overwrites P_t: after the tile's own P V

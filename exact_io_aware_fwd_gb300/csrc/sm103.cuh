@@ -278,6 +278,81 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Whole K-step chains in one asm block.  Step k uses the base descriptors plus constant offsets
+// (16-byte units for shared-memory descriptors, columns for a tensor-memory A operand); the first
+// step overwrites D unless `accumulate` is nonzero, the others accumulate.  The issuing thread
+// shares its SM sub-partition with busy softmax / elementwise warps, where every instruction it
+// issues costs several cycles (measured on GB300: one tcgen05.mma per 64 cycles alone, one per
+// ~120 cycles next to two busy warps), so the chains keep the per-MMA instruction count minimal.
+#define FA_MMA_SS_STEP(AO, BO)                                                     \
+  "add.s64 ra, %1, " #AO ";\n\tadd.s64 rb, %2, " #BO ";\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, q;\n\t"
+#define FA_MMA_TS_STEP(AO, BO)                                                     \
+  "add.u32 ta, %1, " #AO ";\n\tadd.s64 rb, %2, " #BO ";\n\t"                    \
+  "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], rb, %3, q;\n\t"
+#define FA_MMA_HEAD                                                                \
+  "{\n\t.reg .pred p, q;\n\t.reg .b64 ra, rb;\n\t.reg .b32 ta;\n\t"          \
+  "setp.ne.b32 p, %4, 0;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+
+// K-major A and B (S = Q K^T style), K = 64: steps of 32 bytes inside one 128-byte panel.
+__device__ __forceinline__ void mma_ss_kmajor_k64(uint32_t d, uint64_t a, uint64_t b,
+                                                  uint32_t id, uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               FA_MMA_SS_STEP(2, 2) FA_MMA_SS_STEP(4, 4) FA_MMA_SS_STEP(6, 6) "}"
+               :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+// K = 128: two 64-element panels 16 KB apart.
+__device__ __forceinline__ void mma_ss_kmajor_k128(uint32_t d, uint64_t a, uint64_t b,
+                                                   uint32_t id, uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               FA_MMA_SS_STEP(2, 2) FA_MMA_SS_STEP(4, 4) FA_MMA_SS_STEP(6, 6)
+               FA_MMA_SS_STEP(1024, 1024) FA_MMA_SS_STEP(1026, 1026)
+               FA_MMA_SS_STEP(1028, 1028) FA_MMA_SS_STEP(1030, 1030) "}"
+               :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+template <int D>
+__device__ __forceinline__ void mma_ss_kmajor(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                              uint32_t accumulate) {
+  static_assert(D == 64 || D == 128, "K = 64 or 128");
+  if constexpr (D == 64) mma_ss_kmajor_k64(d, a, b, id, accumulate);
+  else mma_ss_kmajor_k128(d, a, b, id, accumulate);
+}
+// A = bf16 pairs in tensor memory, 8 columns (16 K elements) per step; B MN-major, K = 128 rows
+// of 128 bytes: +2048 bytes per step.
+__device__ __forceinline__ void mma_ts_k128_step8(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                                  uint32_t id, uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               FA_MMA_TS_STEP(8, 128) FA_MMA_TS_STEP(16, 256) FA_MMA_TS_STEP(24, 384)
+               FA_MMA_TS_STEP(32, 512) FA_MMA_TS_STEP(40, 640) FA_MMA_TS_STEP(48, 768)
+               FA_MMA_TS_STEP(56, 896) "}"
+               :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+
+// As mma_ts_k128_step8 with A packed per 64-element half: the first 64 K elements in columns
+// [0, 32), the next 64 in [64, 96) (the layout of P^T / dS^T written by two elementwise groups).
+__device__ __forceinline__ void mma_ts_k128_split(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                                  uint32_t id, uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               FA_MMA_TS_STEP(8, 128) FA_MMA_TS_STEP(16, 256) FA_MMA_TS_STEP(24, 384)
+               FA_MMA_TS_STEP(64, 512) FA_MMA_TS_STEP(72, 640) FA_MMA_TS_STEP(80, 768)
+               FA_MMA_TS_STEP(88, 896) "}"
+               :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+// A and B both MN-major over K = 128 rows of 128 bytes: +2048 bytes per step for both.
+__device__ __forceinline__ void mma_ss_mn_k128(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                               uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+               FA_MMA_SS_STEP(128, 128) FA_MMA_SS_STEP(256, 256) FA_MMA_SS_STEP(384, 384)
+               FA_MMA_SS_STEP(512, 512) FA_MMA_SS_STEP(640, 640) FA_MMA_SS_STEP(768, 768)
+               FA_MMA_SS_STEP(896, 896) "}"
+               :: "r"(d), "l"(a), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+
 // The mbarrier receives one arrive once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
