@@ -523,7 +523,7 @@ def run_ours(args, w, world, rank, local):
 
     cpu = None
     if not args.no_cpu_baseline:
-        flops_s, dt, sample = time_oracle_once(w, q, k, v, do, kv)
+        flops_s, dt, sample = time_oracle_once(w, q, k, v, do, extra)
         cpu = {"value": flops_s / dt / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
                "kind": "oracle", "sample": sample, "seconds": dt}
 

@@ -43,3 +43,26 @@ def test_max_over_ranks_gloo(tmp_path):
            "--master-addr=127.0.0.1", "--master-port=29534", str(script)]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
+
+
+def test_cpu_baseline_sample_for_every_workload_kind():
+    """bench.py's oracle sample works for dense, key-padded, block-sparse, GQA and packed
+    variable-length workloads (small copies of each kind)."""
+    import dataclasses
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    from exact_io_aware_fwd_gb300.workloads import BY_NAME, workload_inputs
+
+    small = {"long-causal-1x32x16384x128": dict(H=1, N=300),
+             "ragged-8x12x2000x128": dict(B=2, H=1, N=300, kv_len_range=(100, 300)),
+             "butterfly-1x32x16384x128": dict(H=1, N=300),
+             "gqa-1x32kv8x16384x128": dict(H=4, Hkv=2, N=300),
+             "varlen-16x16x512-4096x128": dict(B=3, H=2, N=300, seqlen_range=(50, 300))}
+    for name, kw in small.items():
+        w = dataclasses.replace(BY_NAME[name], **kw)
+        q, k, v, do, extra = workload_inputs(w)
+        flops, dt, sample = bench.time_oracle_once(w, q, k, v, do, extra)
+        assert flops > 0 and dt > 0 and sample, name
