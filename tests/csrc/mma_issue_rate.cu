@@ -9,7 +9,9 @@
 #include "sm103.cuh"
 using namespace fa;
 
-template <int N, bool TS, bool BMN, int BUSY>
+// CHAIN: issue the MMAs 8 at a time through the library's one-asm K-step chain (N = 128, SS,
+// K-major), as the attention kernels do.
+template <int N, bool TS, bool BMN, int BUSY, bool CHAIN = false>
 __global__ void __launch_bounds__(384, 1) rate_kernel(int iters, long long* out, int* status) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -43,9 +45,13 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int iters, long long* out,
     const uint64_t db = sdesc_sw128(sbase + 32768, 16384, 1024);   // B
     constexpr uint32_t id = idesc_bf16(128, N, false, BMN);
     const long long t0 = clock64();
-    for (int i = 0; i < iters; ++i) {
-      if (TS) mma_ts(tmem + 0, tmem + 256, db, id, i > 0 ? 1u : 0u);
-      else mma_ss(tmem + 0, da, db, id, i > 0 ? 1u : 0u);
+    if (CHAIN) {
+      for (int i = 0; i < iters; i += 8) mma_ss_kmajor_k128(tmem + 0, da, db, id, i > 0 ? 1u : 0u);
+    } else {
+      for (int i = 0; i < iters; ++i) {
+        if (TS) mma_ts(tmem + 0, tmem + 256, db, id, i > 0 ? 1u : 0u);
+        else mma_ss(tmem + 0, da, db, id, i > 0 ? 1u : 0u);
+      }
     }
     const long long t1 = clock64();
     mma_commit(bar);
@@ -58,9 +64,9 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int iters, long long* out,
   if (threadIdx.x < 32) { tc_fence_after(); tmem_dealloc(tmem, 512); }
 }
 
-template <int N, bool TS, bool BMN, int BUSY = 0>
+template <int N, bool TS, bool BMN, int BUSY = 0, bool CHAIN = false>
 void run(const char* name, int iters, long long* d_out, int* d_status) {
-  auto k = rate_kernel<N, TS, BMN, BUSY>;
+  auto k = rate_kernel<N, TS, BMN, BUSY, CHAIN>;
   cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 131072 + 2048);
   k<<<148, 384, 131072 + 2048>>>(iters, d_out, d_status);
   cudaError_t e = cudaDeviceSynchronize();
@@ -90,5 +96,7 @@ int main() {
   run<64, true, true, 2>("TS, +2 busy warps", it, d_out, d_status);
   run<128, true, true, 2>("TS, +2 busy warps", it, d_out, d_status);
   run<128, false, false, 2>("SS, +2 busy warps", it, d_out, d_status);
+  run<128, false, false, 0, true>("SS chain of 8, idle", it, d_out, d_status);
+  run<128, false, false, 2, true>("SS chain of 8, +2 busy", it, d_out, d_status);
   return 0;
 }
