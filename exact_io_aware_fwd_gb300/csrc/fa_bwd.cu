@@ -35,6 +35,8 @@
 //   (((bh * num_qtiles + i) * (d / 4) + g) * 128 + r) * 4 + e,
 // so that 32 consecutive rows of one column group are 512 contiguous bytes and a warp's
 // vector reduction is fully coalesced.
+#include <type_traits>
+
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -523,31 +525,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float* nd = reinterpret_cast<const float*>(sm + L::kDelta + s * 512) + q0;
       const float2 cc = make_float2(c2, c2);
       const bool diag = a.causal && (i == j);
+      // only the causal diagonal tile and a key tile running past the key length need element
+      // masks; every other tile (the test is uniform over the CTA) skips them
+      const bool masked = diag || (j * 128 + 128 > kv_len);
       uint32_t p[kQG / 2];
+      auto p_from_s = [&](auto kMask) {
 #pragma unroll
-      for (int c = 0; c < kQG / 32; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        tmem_wait_ld();
-        reg_fence(sv);
+        for (int c = 0; c < kQG / 32; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tS + 32 * c, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int ql = 32 * c + 4 * e;  // query within this group
-          const float4 l4 = *reinterpret_cast<const float4*>(nl2 + ql);  // -LSE * log2(e)
-          const float2 y0 = fma2(make_float2(__uint_as_float(sv[4 * e]), __uint_as_float(sv[4 * e + 1])),
-                                 cc, make_float2(l4.x, l4.y));
-          const float2 y1 = fma2(make_float2(__uint_as_float(sv[4 * e + 2]), __uint_as_float(sv[4 * e + 3])),
-                                 cc, make_float2(l4.z, l4.w));
-          float x[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
+          for (int e = 0; e < 8; ++e) {
+            const int ql = 32 * c + 4 * e;  // query within this group
+            const float4 l4 = *reinterpret_cast<const float4*>(nl2 + ql);  // -LSE * log2(e)
+            const float2 y0 = fma2(make_float2(__uint_as_float(sv[4 * e]), __uint_as_float(sv[4 * e + 1])),
+                                   cc, make_float2(l4.x, l4.y));
+            const float2 y1 = fma2(make_float2(__uint_as_float(sv[4 * e + 2]), __uint_as_float(sv[4 * e + 3])),
+                                   cc, make_float2(l4.z, l4.w));
+            float x[4] = {ex2(y0.x), ex2(y0.y), ex2(y1.x), ex2(y1.y)};
+            if constexpr (decltype(kMask)::value) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (diag) x[u] = (r <= q0 + ql + u) ? x[u] : 0.f;  // key > query: masked
-            if (!row_live) x[u] = 0.f;
+              for (int u = 0; u < 4; ++u) {
+                if (diag) x[u] = (r <= q0 + ql + u) ? x[u] : 0.f;  // key > query: masked
+                if (!row_live) x[u] = 0.f;
+              }
+            }
+            p[16 * c + 2 * e] = pack_bf16(x[0], x[1]);
+            p[16 * c + 2 * e + 1] = pack_bf16(x[2], x[3]);
           }
-          p[16 * c + 2 * e] = pack_bf16(x[0], x[1]);
-          p[16 * c + 2 * e + 1] = pack_bf16(x[2], x[3]);
         }
-      }
+      };
+      if (masked) p_from_s(std::true_type{});
+      else p_from_s(std::false_type{});
       // P^T over the first half of this group's columns (all of its S^T was read)
       if (kQG == 64) tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
       else tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&p[0]));
