@@ -262,28 +262,52 @@ def oracle_row_block(q, k, v, do, causal, scale, kv_len, rows, block_mask=None):
     return 14.0 * q.shape[1] * float(visible.sum())
 
 
-def cpu_sample_inputs(w, q, k, v, do, kv):
-    """Head 0 of batch 0 (variable-length: of the first sequence; kv is then cu_seqlens)."""
+def cpu_sample_inputs(w, q, k, v, do, kv, i=0):
+    """The i-th (batch, head) slice in order, head 0 first (variable-length: the i-th sequence's
+    head 0; kv is then cu_seqlens): (q, k, v, do, kv_len, n, label) as fp64 arrays plus the key
+    length, the row count and a label; None past the last slice."""
     if w.seqlen_range is not None:
-        s0, s1 = int(kv[0]), int(kv[1])
+        if i >= w.B:
+            return None
+        s0, s1 = int(kv[i]), int(kv[i + 1])
         f = lambda t: t[s0:s1, 0].float().numpy().astype(np.float64)  # noqa: E731
-        n, kv_len = s1 - s0, None
-    else:
-        f = lambda t: t[0, 0].float().numpy().astype(np.float64)  # noqa: E731
-        n, kv_len = w.N, (int(kv[0]) if kv is not None else None)
-    rows_n = min(n, 2048)
-    rows = np.arange(n - rows_n, n)  # the last rows: the most keys under a causal mask
-    return f(q), f(k), f(v), f(do), kv_len, rows
+        return f(q), f(k), f(v), f(do), None, s1 - s0, f"sequence {i} head 0"
+    if i >= w.B * w.H:
+        return None
+    b, h = divmod(i, w.H)
+    hk = h // (w.H // w.kv_heads)
+    fq = lambda t: t[b, h].float().numpy().astype(np.float64)  # noqa: E731
+    fk = lambda t: t[b, hk].float().numpy().astype(np.float64)  # noqa: E731
+    kv_len = int(kv[b]) if kv is not None else None
+    return fq(q), fk(k), fk(v), fq(do), kv_len, w.N, f"(b,h)=({b},{h})"
 
 
-def time_oracle_once(w, q, k, v, do, kv):
-    qs, ks, vs, dos, kv_len, rows = cpu_sample_inputs(w, q, k, v, do, kv)
-    t0 = time.perf_counter()
+def time_oracle_once(w, q, k, v, do, kv, min_seconds=0.0, block=2048):
+    """The oracle on blocks of `block` query rows, from a head's last rows backwards (the most
+    keys under a causal mask) and head after head, until at least `min_seconds` have passed (one
+    block when 0).  Returns (credited FLOPs, seconds, description of the sample)."""
     mask = workload_block_mask(w)
-    flops = oracle_row_block(qs, ks, vs, dos, w.causal, w.scale, kv_len, rows,
-                             None if mask is None else mask.numpy())
-    dt = time.perf_counter() - t0
-    return flops, dt, f"(b,h)=(0,0), query rows {rows[0]}..{rows[-1]} of N={w.N}: O, LSE, dQ and their dK, dV contributions"
+    mask = None if mask is None else mask.numpy()
+    flops, dt, parts = 0.0, 0.0, []
+    i = 0
+    while True:
+        sl = cpu_sample_inputs(w, q, k, v, do, kv, i)
+        if sl is None:
+            break
+        qs, ks, vs, dos, kv_len, n, label = sl
+        lo = n
+        while lo > 0 and (dt < min_seconds or not parts and lo == n):
+            rows = np.arange(max(0, lo - block), lo)
+            t0 = time.perf_counter()
+            flops += oracle_row_block(qs, ks, vs, dos, w.causal, w.scale, kv_len, rows, mask)
+            dt += time.perf_counter() - t0
+            lo = rows[0]
+        parts.append(f"{label} query rows {lo}..{n - 1} of {n}")
+        if dt >= min_seconds:
+            break
+        i += 1
+    desc = "; ".join(parts) + ": O, LSE, dQ and their dK, dV contributions"
+    return flops, dt, desc
 
 
 def cpu_cores():
@@ -523,7 +547,7 @@ def run_ours(args, w, world, rank, local):
 
     cpu = None
     if not args.no_cpu_baseline:
-        flops_s, dt, sample = time_oracle_once(w, q, k, v, do, extra)
+        flops_s, dt, sample = time_oracle_once(w, q, k, v, do, extra, min_seconds=10.0)
         cpu = {"value": flops_s / dt / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
                "kind": "oracle", "sample": sample, "seconds": dt}
 
