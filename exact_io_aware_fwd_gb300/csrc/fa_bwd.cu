@@ -482,35 +482,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     // dQ_i (query row r of the tile, this group's columns) into the fp32 accumulator: load,
     // release the tensor memory (dP_{i+1} waits for it), then the atomics, which overlap dP_{i+1}
+    // The atomics of the second half of this thread's dQ columns wait until dS has been handed
+    // to the MMA thread (after ds_full), so that they overlap dK += dS^T Q and dQ = dS K instead
+    // of delaying dS; the values wait in registers (dQ must leave tensor memory before dP(i+1)
+    // overwrites it, but the additions can come later).
+    constexpr int kGroups4 = kDC / 4;       // 4-column groups of this thread's dQ columns
+#ifndef FA_DQ_LATE64
+#define FA_DQ_LATE64 0
+#endif
+#ifndef FA_DQ_LATE128
+#define FA_DQ_LATE128 8
+#endif
+    // of which issued after dS.  Measured on GB300 (dK/dV kernel): d = 128 with 0 / 4 / 8 / 12 of
+    // 16 deferred: 4.90 / 4.28 / 4.27 / 4.88 ms on long-causal 1x32x16384, 2.98 / 2.45 / 2.38 /
+    // 2.74 ms on causal 16x16x4096 (12 needs 163 registers); d = 64 with 0 / 4 / 8 of 8: 0.932 /
+    // 0.977 / 1.047 ms on 64x16x1024 (there the atomics are a smaller share than the MMA issue).
+    constexpr int kLate = (D == 128) ? FA_DQ_LATE128 : FA_DQ_LATE64;
+    uint32_t dq_late[4 * (kLate > 0 ? kLate : 1)];
+    float* late_tile = nullptr;
     auto drain = [&](int it, int qh, int qt) -> bool {  // (qh, qt): query head, tile of it
       if (!mbar_wait_warp(dq_full, it & 1, ctl)) return false;
       tc_fence_after();
       float* tile =
           a.dq_acc + (static_cast<size_t>(ws_head(qh)) * a.ws_tiles + ws_tile0 + qt) * 128 * D;
-      const int g0 = (kDC / 4) * grp;  // first 4-column group of this group's columns
-      uint32_t va[32], vb[32];
-      if (kDC >= 32) tmem_ld32(tDQ, va);
-      if (kDC == 64) tmem_ld32(tDQ + 32, vb);
-      if (kDC == 16) tmem_ld16(tDQ, *reinterpret_cast<uint32_t(*)[16]>(&va[0]));
+      const int g0 = kGroups4 * grp;  // first 4-column group of this group's columns
+      uint32_t v[kDC];
+      if constexpr (kDC == 64) {
+        tmem_ld32(tDQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_ld32(tDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      } else if constexpr (kDC == 32) {
+        tmem_ld32(tDQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      } else {
+        tmem_ld16(tDQ, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+      }
       tmem_wait_ld();
-      reg_fence(va);
-      if (kDC == 64) reg_fence(vb);
+      reg_fence(v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
 #pragma unroll
-      for (int g = 0; g < (kDC >= 32 ? 8 : 4); ++g)
-        red_add_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(va[4 * g]),
-                   __uint_as_float(va[4 * g + 1]), __uint_as_float(va[4 * g + 2]),
-                   __uint_as_float(va[4 * g + 3]));
-      if (kDC == 64) {
+      for (int g = 0; g < kGroups4 - kLate; ++g)
+        red_add_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
+                   __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                   __uint_as_float(v[4 * g + 3]));
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-          red_add_v4(tile + ((g0 + 8 + g) * 128 + r) * 4, __uint_as_float(vb[4 * g]),
-                     __uint_as_float(vb[4 * g + 1]), __uint_as_float(vb[4 * g + 2]),
-                     __uint_as_float(vb[4 * g + 3]));
-      }
+      for (int e = 0; e < 4 * kLate; ++e) dq_late[e] = v[4 * (kGroups4 - kLate) + e];
+      late_tile = tile + (g0 + kGroups4 - kLate) * 128 * 4;
       return true;
+    };
+    auto drain_late = [&]() {  // the deferred atomics of the last drain, if any
+      if (late_tile == nullptr) return;
+#pragma unroll
+      for (int g = 0; g < kLate; ++g)
+        red_add_v4(late_tile + (g * 128 + r) * 4, __uint_as_float(dq_late[4 * g]),
+                   __uint_as_float(dq_late[4 * g + 1]), __uint_as_float(dq_late[4 * g + 2]),
+                   __uint_as_float(dq_late[4 * g + 3]));
+      late_tile = nullptr;
     };
 
     bool ok = true;
@@ -608,10 +635,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
+      if (kWithDQ) drain_late();  // dQ(it - 1)'s deferred additions overlap dK / dQ(it)
       h_prev = h;
       i_prev = i;
     }
-    if (kWithDQ && ok && nIt > 0) ok = drain(nIt - 1, h_prev, i_prev);
+    if (kWithDQ) drain_late();  // (an aborted loop may leave one pending)
+    if (kWithDQ && ok && nIt > 0) {
+      ok = drain(nIt - 1, h_prev, i_prev);
+      if (ok) drain_late();
+    }
 
     // ---- epilogue: the 64-column panels of dV and scale * dK (bf16, swizzled, over the V or K
     // tile in smem, which no MMA reads any more) are shared out over the groups; one TMA store
