@@ -508,7 +508,7 @@ def run_ours(args, w, world, rank, local):
 
         def e2e_step():
             ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout,
-                   deterministic=det, block_index=index)
+                   deterministic=det, block_index=index, graph=True)
 
         for _ in range(2):
             e2e_step()

@@ -783,9 +783,7 @@ cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   using L = BwdLayout<D>;
   constexpr uint32_t kMaxSmem = 232448;  // 227 KB, the per-block opt-in limit of sm_100-family GPUs
   const uint32_t smem = (L::kBytes + 1024 <= kMaxSmem) ? L::kBytes + 1024 : kMaxSmem;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel<D, kWithDQ, kSparse, kVarlen>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem_limit<bwd_dkdv_kernel<D, kWithDQ, kSparse, kVarlen>>(smem);
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   // one CTA per (b, key/value head, key tile)

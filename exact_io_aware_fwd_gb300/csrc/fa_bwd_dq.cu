@@ -393,9 +393,7 @@ cudaError_t launch_dq_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   // tcgen05.alloc: ask for enough shared memory (d = 64 needs less than half an SM's) that one
   // CTA fills the SM.
   const uint32_t smem = L::kBytes + 1024 < 120u * 1024u ? 120u * 1024u : L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, kSparse, kVarlen>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem_limit<bwd_dq_kernel<D, kSparse, kVarlen>>(smem);
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qtiles) * static_cast<unsigned>(a.BH);

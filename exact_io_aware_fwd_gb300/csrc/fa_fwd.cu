@@ -531,9 +531,7 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
                          const CUtensorMap& to, FwdArgs a, cudaStream_t st) {
   using L = FwdLayout<D>;
   const uint32_t smem = L::kBytes + 1024;
-  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, kSparse, kVarlen>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem_limit<fwd_kernel<D, kSparse, kVarlen>>(smem);
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qblocks) * static_cast<unsigned>(a.BH);

@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer (fa_api.cu) and the kernel translation units.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
@@ -102,6 +103,21 @@ struct Workspace {
   size_t dq_acc_off, neg_lse2_off, neg_delta_off, total;
 };
 Workspace workspace_layout(int BH, int N, int d);
+
+// Raises kernel K's dynamic shared-memory limit once per device (the attribute persists; setting
+// it on every launch would also be a non-stream call inside a captured CUDA graph).
+template <auto K>
+cudaError_t ensure_smem_limit(uint32_t bytes) {
+  static std::atomic<uint64_t> done{0};  // bit d: set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(K, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Launchers return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
