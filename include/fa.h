@@ -172,7 +172,8 @@ fa_status fa_bwd_varlen(const void* Q, const void* K, const void* V, const void*
  * number of fa_fwd_block_sparse / fa_bwd_block_sparse calls with the same N.
  *
  * fa_block_index_size: bytes of the index for sequence length N and mask_heads masks
- *   (12 * T^2 + 12 * T bytes per mask, T = ceil(N / 128)); 0 for invalid sizes.
+ *   (4 * (2 * T^2 + 3 * T + Tb * (T + 1)) bytes per mask, about 10 * T^2, with T = ceil(N / 128)
+ *   and Tb = ceil(T / 2)); 0 for invalid sizes.
  * fa_block_index_build: block_mask is DEVICE uint8 [mask_heads][T][T], row = query tile,
  *   column = key tile, nonzero = kept.  index: DEVICE memory of at least
  *   fa_block_index_size(N, mask_heads) bytes, 16-byte aligned, owned by the caller; it holds the

@@ -76,3 +76,42 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         fa.load_library(str(tmp_path / "missing.so"))
+
+
+def test_invalid_arguments_of_the_extensions(lib):
+    """Grouped-query, variable-length and block-sparse entry points reject bad arguments before
+    touching the device (this machine may have none)."""
+    p = ctypes.c_void_p(0x10000)
+    null = ctypes.c_void_p(0)
+    mis = ctypes.c_void_p(0x10004)
+    # grouped-query: Hkv must divide H
+    assert lib.fa_fwd_gqa(p, p, p, p, p, 1, 6, 4, 128, 64, 0, -1.0, null, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_gqa(p, p, p, p, p, 1, 6, 0, 128, 64, 0, -1.0, null, null) == fa.FA_ERR_INVALID_ARG
+    bargs = [p] * 9 + [1, 6, 4, 128, 64, 0, -1.0, null, 0, p, 1 << 20, null]
+    assert lib.fa_bwd_gqa(*bargs) == fa.FA_ERR_INVALID_ARG
+    # variable-length: offsets required, sizes checked, an empty batch is a no-op
+    assert lib.fa_fwd_varlen(p, p, p, p, p, null, 2, 128, 256, 4, 4, 64, 0, -1.0, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_varlen(p, p, p, p, p, p, 2, 128, -1, 4, 4, 64, 0, -1.0, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_varlen(p, p, p, p, p, p, 2, 0, 256, 4, 4, 64, 0, -1.0, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_varlen(p, p, p, p, p, p, 2, 128, 256, 4, 3, 64, 0, -1.0, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_varlen(null, null, null, null, null, p, 2, 128, 0, 4, 4, 64, 0, -1.0, null) == fa.FA_OK
+    assert lib.fa_bwd_varlen_workspace_size(0, 256, 4, 64) == 0
+    assert lib.fa_bwd_varlen_workspace_size(2, 256, 4, 96) == 0
+    # ceil(256 / 128) + 2 = 4 tiles of 128 rows per head: dQ fp32 + two row statistics
+    assert lib.fa_bwd_varlen_workspace_size(2, 256, 4, 64) >= 4 * 4 * 128 * (64 + 2) * 4
+    vargs = [p] * 9 + [p, 2, 128, 256, 4, 4, 64, 0, -1.0, 0]
+    assert lib.fa_bwd_varlen(*vargs, null, 1 << 20, null) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd_varlen(*vargs, p, 16, null) == fa.FA_ERR_WORKSPACE
+    # block-sparse: index size, build arguments, mask heads 1 or H, aligned index
+    assert lib.fa_block_index_size(0, 1) == 0 and lib.fa_block_index_size(1000, 0) == 0
+    t = (1000 + 127) // 128
+    tb = (t + 1) // 2
+    assert lib.fa_block_index_size(1000, 2) == 2 * 4 * (2 * t * t + 3 * t + tb * (t + 1))
+    assert lib.fa_block_index_build(null, 1000, 1, p, 1 << 20, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_block_index_build(p, 1000, 1, mis, 1 << 20, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_block_index_build(p, 1000, 1, p, 16, null) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_fwd_block_sparse(p, p, p, p, p, 1, 4, 1000, 64, 0, -1.0, null, p, 3, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_block_sparse(p, p, p, p, p, 1, 4, 1000, 64, 0, -1.0, null, mis, 1, null) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_fwd_block_sparse(p, p, p, p, p, 1, 4, 1000, 64, 0, -1.0, null, null, 1, null) == fa.FA_ERR_INVALID_ARG
+    sargs = [p] * 9 + [1, 4, 1000, 64, 0, -1.0, null, p, 2, 0]
+    assert lib.fa_bwd_block_sparse(*sargs, p, 1 << 20, null) == fa.FA_ERR_INVALID_ARG
