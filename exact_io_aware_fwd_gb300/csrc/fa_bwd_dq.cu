@@ -18,6 +18,8 @@
 //   dQ += dS K_j       (A = dS from tensor memory, B = K_j MN-major) -> [384, 384 + D)
 // Block-sparse (kSparse): the key tiles are the query tile's kept ones (an ascending list from the
 // block index, cut at the causal / key-length limit).
+#include <type_traits>
+
 #include "fa_internal.h"
 #include "sm103.cuh"
 
@@ -273,27 +275,33 @@ __global__ void __launch_bounds__(384, 1)
       const int k0 = kt * 128 + 64 * grp;  // first key of this group's columns
       // keys >= klim are masked (causal: key > query; padding: key >= kv_len)
       const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;
-      const bool masked = (k0 + 64 > klim);
+      // element masks only where some row of the warp needs them (the causal diagonal, the
+      // key-length tail); the test is uniform over the warp, so the loop is chosen once
+      const bool masked = __any_sync(0xffffffffu, k0 + 64 > klim);
       uint32_t p[32];
+      auto p_from_s = [&](auto kMask) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32];
-        tmem_ld32(tS + 32 * c, sv);
-        tmem_wait_ld();
-        reg_fence(sv);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32];
+          tmem_ld32(tS + 32 * c, sv);
+          tmem_wait_ld();
+          reg_fence(sv);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float2 y = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
-                                cc, nl);
-          float x0 = ex2(y.x), x1 = ex2(y.y);
-          if (masked) {
-            const int kk = k0 + 32 * c + 2 * e;
-            x0 = (kk < klim) ? x0 : 0.f;
-            x1 = (kk + 1 < klim) ? x1 : 0.f;
+          for (int e = 0; e < 16; ++e) {
+            const float2 y = fma2(make_float2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])),
+                                  cc, nl);
+            float x0 = ex2(y.x), x1 = ex2(y.y);
+            if constexpr (decltype(kMask)::value) {
+              const int kk = k0 + 32 * c + 2 * e;
+              x0 = (kk < klim) ? x0 : 0.f;
+              x1 = (kk + 1 < klim) ? x1 : 0.f;
+            }
+            p[16 * c + e] = pack_bf16(x0, x1);
           }
-          p[16 * c + e] = pack_bf16(x0, x1);
         }
-      }
+      };
+      if (masked) p_from_s(std::true_type{});
+      else p_from_s(std::false_type{});
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_read);  // S(j) fully read: S(j+1) may overwrite it
