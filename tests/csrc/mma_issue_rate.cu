@@ -96,6 +96,9 @@ int main() {
   run<64, true, true, 2>("TS, +2 busy warps", it, d_out, d_status);
   run<128, true, true, 2>("TS, +2 busy warps", it, d_out, d_status);
   run<128, false, false, 2>("SS, +2 busy warps", it, d_out, d_status);
+  run<128, false, false, 1>("SS, +1 busy warp", it, d_out, d_status);
+  run<256, false, false, 1>("SS, +1 busy warp", it, d_out, d_status);
+  run<256, false, false, 2>("SS, +2 busy warps", it, d_out, d_status);
   run<128, false, false, 0, true>("SS chain of 8, idle", it, d_out, d_status);
   run<128, false, false, 2, true>("SS chain of 8, +2 busy", it, d_out, d_status);
   return 0;
