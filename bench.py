@@ -467,48 +467,29 @@ def run_ours(args, w, world, rank, local):
     # ---- end to end through the public API with host buffers: pinned host inputs in, pinned
     # host outputs (O, LSE, dQ, dK, dV) out, copies overlapped with compute over head chunks
     e2e = None
-    if not args.no_e2e and (varlen or gqa):
-        # host buffers in and out around the same two calls, on one stream (no chunking)
-        hin = [t.pin_memory() for t in (q, k, v, do)]
-        hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
-        h2d = sum(t.numel() * t.element_size() for t in hin)
-        d2h = sum(t.numel() * t.element_size() for t in hout)
+    if not args.no_e2e:
+        from exact_io_aware_fwd_gb300.pipeline import HostAttention, VarlenHostAttention
 
-        def e2e_step():
-            for dst, src in zip((qd, kd, vd, dod), hin):
-                dst.copy_(src, non_blocking=True)
-            step_two()
-            for dst, src in zip(hout, (o, lse, dq, dk, dv)):
-                dst.copy_(src, non_blocking=True)
-
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        a, bv = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        bv.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        e2e_ms = max_over_ranks(a.elapsed_time(bv), world) / args.steps
-        e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "chunks": 1}
-        assert fa.fa_get_error() == fa.FA_OK
-    elif not args.no_e2e:
-        from exact_io_aware_fwd_gb300.pipeline import HostAttention
-
-        ha = HostAttention(B, H, N, d, device=dev)
         hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
-        hout = {name: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
-                for name in ("O", "dQ", "dK", "dV")}
-        hout["LSE"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        h2d, d2h = ha.transfer_bytes(with_kv=kv is not None)
+        if varlen:
+            ha = VarlenHostAttention(extra, H, d, device=dev, Hkv=k.shape[1])
+            h2d, d2h = ha.transfer_bytes()
 
-        def e2e_step():
-            ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout,
-                   deterministic=det, block_index=index, graph=True)
+            def e2e_step():
+                ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, out=hout,
+                       deterministic=det, graph=True)
+        else:
+            ha = HostAttention(B, H, N, d, device=dev, Hkv=k.shape[1])
+            h2d, d2h = ha.transfer_bytes(with_kv=kv is not None)
+
+            def e2e_step():
+                ha.run(hq, hk, hv, hdo, causal=w.causal, scale=w.scale, kv_lens=kv, out=hout,
+                       deterministic=det, block_index=index, graph=True)
+        hout = {"O": torch.empty(q.shape, dtype=torch.bfloat16).pin_memory(),
+                "dQ": torch.empty(q.shape, dtype=torch.bfloat16).pin_memory(),
+                "dK": torch.empty(k.shape, dtype=torch.bfloat16).pin_memory(),
+                "dV": torch.empty(k.shape, dtype=torch.bfloat16).pin_memory(),
+                "LSE": torch.empty(lse_shape, dtype=torch.float32).pin_memory()}
 
         for _ in range(2):
             e2e_step()
