@@ -185,8 +185,46 @@ def ingest_ncu(csv_path, workload, command):
         f.write("\n")
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes on the driver's
+    libnvidia-ml (no Python package needed).  None of these calls changes any GPU setting."""
+
+    CLOCK_SM = 1
+    # clock event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x40: "sw_thermal_slowdown",
+               0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown"}
+
+    def __init__(self, index):
+        import ctypes
+
+        self.c = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML device")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        v = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) != 0:
+            raise OSError("no max clock")
+        self.max_sm = v.value
+
+    def sample(self):
+        v, r = self.c.c_uint(), self.c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.c.byref(v)) != 0:
+            return None
+        if self.reasons_fn(self.h, self.c.byref(r)) != 0:
+            return None
+        return v.value, r.value
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """SM clock and throttle reasons sampled during the timed region: every 10 ms through NVML
+    (samples outside [mark_start, mark_end] are dropped), else every 200 ms through nvidia-smi
+    (all samples kept)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -194,12 +232,22 @@ class ClockSampler:
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
-        self.rows = []
+        self.rows = []       # nvidia-smi rows
+        self.samples = []    # NVML (time, sm_mhz, reason bits)
+        self.window = None
         self._stop = threading.Event()
         self._proc = None
         self._thread = None
+        try:
+            self._nvml = _Nvml(gpu_index)
+        except (OSError, AttributeError):
+            self._nvml = None
 
     def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return
         try:
             self._proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
@@ -211,13 +259,25 @@ class ClockSampler:
         self._thread = threading.Thread(target=self._read, daemon=True)
         self._thread.start()
 
+    def _poll(self):
+        while not self._stop.is_set():
+            got = self._nvml.sample()
+            if got is not None:
+                self.samples.append((time.perf_counter(), *got))
+            time.sleep(0.01)
+
     def _read(self):
         for line in self._proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) >= 8:
                 self.rows.append(parts)
 
+    def mark(self, t_start, t_end):
+        """The host-clock interval of the timed region (first launch .. final synchronize)."""
+        self.window = (t_start, t_end)
+
     def stop(self):
+        self._stop.set()
         if self._proc is not None:
             self._proc.terminate()
             try:
@@ -228,6 +288,17 @@ class ClockSampler:
             self._thread.join(timeout=5)
 
     def summary(self):
+        if self._nvml is not None:
+            lo, hi = self.window if self.window else (float("-inf"), float("inf"))
+            inside = [(mhz, bits) for t, mhz, bits in self.samples if lo <= t <= hi]
+            if not inside:
+                return {"sm_mhz": None, "sm_max_mhz": self._nvml.max_sm, "reasons": ["unsampled"],
+                        "samples": 0, "source": "nvml"}
+            reasons = sorted({name for _, bits in inside for bit, name in _Nvml.REASONS.items()
+                              if bits & bit})
+            return {"sm_mhz": statistics.median(m for m, _ in inside),
+                    "sm_max_mhz": self._nvml.max_sm, "reasons": reasons,
+                    "samples": len(inside), "source": "nvml, every 10 ms"}
         if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
@@ -236,7 +307,7 @@ class ClockSampler:
         reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v.strip() == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(self.rows), "source": "nvidia-smi, every 200 ms"}
 
 
 # ------------------------------------------------------------------------------- oracle timing
@@ -447,11 +518,13 @@ def run_ours(args, w, world, rank, local):
     time.sleep(0.3)  # let the sampler start before the timed region
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    h_start = time.perf_counter()
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(h_start, time.perf_counter())
     clocks.stop()
     barrier(world)
     st = fa.fa_get_error()
