@@ -53,7 +53,36 @@ namespace {
 #ifndef FA_ROUNDED_SUM
 #define FA_ROUNDED_SUM 0
 #endif
+// Software exp2 (FlashAttention-4's idea of moving part of the exponentials off the MUFU pipe,
+// page two, section "FlashAttention-4"): N > 0 sends one pair of every N in the unmasked softmax
+// loop through exp2_poly2 on the FMA pipe instead of MUFU ex2.  Off: measured slower on GB300
+// (MUFU is not the ceiling; the extra instructions crowd the MMA-issuing thread).
+#ifndef FA_SOFT_EXP2
+#define FA_SOFT_EXP2 0
+#endif
 constexpr float kRescaleThreshold = FA_RESCALE_THRESHOLD;
+
+// 2^x for a pair, x <= 0: 2^x = 2^n * 2^f with n = round(x), f = x - n in [-1/2, 1/2].  Adding
+// 1.5 * 2^23 rounds x to an integer held in the low mantissa bits of t; 2^f comes from a degree-3
+// polynomial (least-squares fit of 2^f on Chebyshev nodes of [-1/2, 1/2], relative error below
+// 8e-5, far under the 2^-9 of the bf16 rounding that P gets next), and 2^n is applied by adding
+// n << 23 to the polynomial's exponent field (t << 23 is exactly n << 23: the low 9 bits of
+// 1.5 * 2^23's pattern are zero).  x is clamped at -126 so that the exponent stays in range.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -126.f);
+  x.y = fmaxf(x.y, -126.f);
+  const float2 magic = make_float2(12582912.f, 12582912.f);
+  const float2 t = add2(x, magic);
+  const float2 r = add2(t, make_float2(-12582912.f, -12582912.f));  // round(x), exact
+  const float2 f = fma2(r, make_float2(-1.f, -1.f), x);               // x - round(x), exact
+  float2 q = fma2(make_float2(0.05508868396282196f, 0.05508868396282196f), f,
+                  make_float2(0.24260404706001282f, 0.24260404706001282f));
+  q = fma2(q, f, make_float2(0.6932762265205383f, 0.6932762265205383f));
+  q = fma2(q, f, make_float2(0.9999289512634277f, 0.9999289512634277f));
+  const uint32_t e0 = __float_as_uint(q.x) + __float_as_uint(t.x) * 8388608u;
+  const uint32_t e1 = __float_as_uint(q.y) + __float_as_uint(t.y) * 8388608u;
+  return make_float2(__uint_as_float(e0), __uint_as_float(e1));
+}
 constexpr float kLn2 = 0.693147180559945309f;
 
 template <int D>
@@ -413,7 +442,15 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 64; ++c) {
           const float2 x = fma2(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
                                 cc, nm);
-          const float x0 = ex2(x.x), x1 = ex2(x.y);
+          float x0, x1;
+          if (FA_SOFT_EXP2 > 0 && c % (FA_SOFT_EXP2 > 0 ? FA_SOFT_EXP2 : 1) == FA_SOFT_EXP2 - 1) {
+            const float2 e = exp2_poly2(x);
+            x0 = e.x;
+            x1 = e.y;
+          } else {
+            x0 = ex2(x.x);
+            x1 = ex2(x.y);
+          }
           p[c] = pack_bf16(x0, x1);
           sumv[c & 1] = add2(sumv[c & 1], make_float2(x0, x1));
           if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
