@@ -1,5 +1,6 @@
 // C-ABI entry points (declared in include/fa.h): argument validation, TMA tensor-map encoding,
 // kernel launches and the device status word.  Nothing here allocates device memory.
+#include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -15,41 +16,42 @@ __device__ int g_fa_status = 0;  // first device-side error since the last fa_ge
 
 constexpr int kMaxDevices = 64;
 
+// Per-device address of the status word (looked up once per device; calls from several host
+// threads may race to look it up, and all of them store the same value).
 int* status_ptr() {
-  static int* ptrs[kMaxDevices] = {nullptr};
+  static std::atomic<int*> ptrs[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
-  }
-  return ptrs[dev];
+  int* cached = ptrs[dev].load(std::memory_order_acquire);
+  if (cached != nullptr) return cached;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_fa_status) != cudaSuccess) return nullptr;
+  ptrs[dev].store(static_cast<int*>(p), std::memory_order_release);
+  return static_cast<int*>(p);
 }
 
 uint64_t wait_timeout_ns() {
-  static uint64_t ns = 0;
-  if (ns == 0) {
+  static const uint64_t ns = [] {  // initialised once, thread-safely
     uint64_t ms = 2000;  // a single pipeline wait is normally a few microseconds
     if (const char* e = std::getenv("FA_WAIT_TIMEOUT_MS")) {
       const long v = std::strtol(e, nullptr, 10);
       if (v > 0) ms = static_cast<uint64_t>(v);
     }
-    ns = ms * 1000000ull;
-  }
+    return ms * 1000000ull;
+  }();
   return ns;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {  // looked up once, thread-safely
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
