@@ -21,7 +21,7 @@ def test_mma_issue_rate(tmp_path):
                    check=True, capture_output=True)
     out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, timeout=120).stdout
     lines = out.strip().splitlines()
-    assert len(lines) == 17, out
+    assert len(lines) == 20, out
     for line in lines:
         assert "no error st=0" in line, line
     idle_128 = [ln for ln in lines if "N=128" in ln and "busy" not in ln]
