@@ -280,10 +280,11 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
 }
 // Whole K-step chains in one asm block.  Step k uses the base descriptors plus constant offsets
 // (16-byte units for shared-memory descriptors, columns for a tensor-memory A operand); the first
-// step overwrites D unless `accumulate` is nonzero, the others accumulate.  The issuing thread
-// shares its SM sub-partition with busy softmax / elementwise warps, where every instruction it
-// issues costs several cycles (measured on GB300: one tcgen05.mma per 64 cycles alone, one per
-// ~120 cycles next to two busy warps), so the chains keep the per-MMA instruction count minimal.
+// step overwrites D unless `accumulate` is nonzero, the others accumulate.  Keeping the issuing
+// thread's instructions between MMAs to two adds per step made the forward 3-4% faster on GB300.
+// (Measured there: one tcgen05.mma per 64 cycles at N = 128 with the sub-partition otherwise
+// idle; ~120 next to two warps issuing a scalar fp32 instruction every cycle, while packed
+// FFMA2, MUFU, integer and tensor-memory-load traffic leave the rate at 64.)
 #define FA_MMA_SS_STEP(AO, BO)                                                     \
   "add.s64 ra, %1, " #AO ";\n\tadd.s64 rb, %2, " #BO ";\n\t"                    \
   "tcgen05.mma.cta_group::1.kind::f16 [%0], ra, rb, %3, q;\n\t"
