@@ -167,15 +167,27 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   const int q = i * 128 + r;
   if (q >= tr.n) return;
   const float* tile = acc + tr.ws_tile * 128 * D;
-  for (int cp = threadIdx.x >> 7; cp < D / 8; cp += 2) {
-    const float4 a0 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp) * 128 + r) * 4));
-    const float4 a1 = __ldg(reinterpret_cast<const float4*>(tile + ((2 * cp + 1) * 128 + r) * 4));
-    uint4 o;
-    o.x = pack_bf16(a0.x * scale, a0.y * scale);
-    o.y = pack_bf16(a0.z * scale, a0.w * scale);
-    o.z = pack_bf16(a1.x * scale, a1.y * scale);
-    o.w = pack_bf16(a1.z * scale, a1.w * scale);
-    *reinterpret_cast<uint4*>(dQ + tr.row(q) * D + cp * 8) = o;
+  // 16 columns of row r per step: four 16-byte loads (a warp reads 32 consecutive rows of one
+  // 4-column group, 512 contiguous bytes each), then the whole 32-byte sector of bf16 output
+  // written by this thread (two 16-byte stores back to back), so no output sector is assembled
+  // from the partial writes of two threads
+  const float2 sc = make_float2(scale, scale);
+  for (int ch = threadIdx.x >> 7; ch < D / 16; ch += 2) {
+    float4 a[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+      a[g] = __ldg(reinterpret_cast<const float4*>(tile + ((4 * ch + g) * 128 + r) * 4));
+    uint32_t w[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const float2 lo = mul2(make_float2(a[g].x, a[g].y), sc);
+      const float2 hi = mul2(make_float2(a[g].z, a[g].w), sc);
+      w[2 * g] = pack_bf16(lo.x, lo.y);
+      w[2 * g + 1] = pack_bf16(hi.x, hi.y);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(dQ + tr.row(q) * D + ch * 16);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
