@@ -422,8 +422,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA: +2 KB rows)
         ts_chain(tmem + L::kColDV, tmem + L::kColS, desc_do(it), it > 0 ? 1u : 0u);
-        mma_commit(&do_empty[it & 1]);
       };
+      // dO_i is read by dP(i) and dV(i): its stage is released after whichever is issued last
+      auto release_do = [&](int it) { mma_commit(&do_empty[it & 1]); };
       auto issue_dK_dQ = [&](int it) {
         ts_chain(tmem + L::kColDK, tmem + L::kColDP, desc_q(it), it > 0 ? 1u : 0u);  // dK += dS^T Q_i
         mma_commit(&q_empty[it & 1]);
@@ -449,6 +450,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok) {
         tc_fence_after();
         issue_dV(0);
+        release_do(0);  // dP(0) went first
         if (nIt > 1 && (ok = wait_q(1))) {
           tc_fence_after();
           issue_S(1);
@@ -459,12 +461,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         issue_dK_dQ(it);
         if (it + 1 < nIt) {
-          if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl))) break;
+          // dV(i+1) reads dO(i+1): its copy must have landed (P(i+1) does not depend on it)
+          if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl) && wait_do(it + 1))) break;
           tc_fence_after();
           issue_dV(it + 1);
-          if (!(ok = wait_do(it + 1) && (!kWithDQ || mbar_wait(dq_empty, it & 1, ctl)))) break;
+          if (kWithDQ && !(ok = mbar_wait(dq_empty, it & 1, ctl))) break;
           tc_fence_after();
           issue_dP(it + 1);
+          release_do(it + 1);
           if (it + 2 < nIt) {
             if (!(ok = wait_q(it + 2))) break;
             tc_fence_after();

@@ -1,0 +1,44 @@
+"""Back-to-back backward calls on a full-size causal shape give bit-identical dK and dV (and dQ
+through the deterministic entry point).  dK and dV accumulate in tensor memory in a fixed order, so
+any difference between calls is a synchronisation error: this guards against a dK/dV kernel that
+issued dV(i) before the copy of dO_i had landed (with the L2 flushed between calls, so that the
+copies are slow, that kernel gave a differing dV in about one call in 60)."""
+
+import pytest
+import torch
+
+from exact_io_aware_fwd_gb300.workloads import BY_NAME, workload_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import exact_io_aware_fwd_gb300 as fa
+
+    fa.build()
+    fa.load_library()
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_back_to_back_backward_calls_agree_bitwise(deterministic):
+    import exact_io_aware_fwd_gb300 as fa
+
+    w = BY_NAME["causal-16x16x4096x128"]
+    dev = torch.device("cuda:0")
+    q, k, v, do, _ = (t.to(dev) if t is not None else None for t in workload_inputs(w))
+    o, lse = fa.fa_fwd(q, k, v, causal=True)
+    ws = fa.workspace_for(q)
+    bwd = fa.fa_bwd_deterministic if deterministic else fa.fa_bwd
+    first = bwd(q, k, v, o, do, lse, causal=True, workspace=ws)
+    checked = (0, 1, 2) if deterministic else (1, 2)  # dQ, dK, dV
+    flags = []  # one small device tensor per call: no synchronisation between calls
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than the 129 MB L2
+    for _ in range(120):
+        flush.zero_()  # each call's loads come from DRAM, as after an idle device
+        out = bwd(q, k, v, o, do, lse, causal=True, workspace=ws)
+        flags.append(torch.stack([(out[i] != first[i]).any() for i in checked]))
+        del out
+    differing = torch.stack(flags).cpu()
+    assert fa.fa_get_error() == fa.FA_OK
+    assert not differing.any(), differing.nonzero().tolist()
