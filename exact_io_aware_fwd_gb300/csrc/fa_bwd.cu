@@ -391,7 +391,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // Issue order (software-pipelined over query tiles): S(0), dP(0), dV(0), S(1), then per
       // tile i: dK(i), dQ(i) | dV(i+1), dP(i+1) | S(i+2).  The tensor pipe always has the next
       // tile's work queued while the P/dS warpgroups compute, and dV(i+1) covers the drain of
-      // dQ(i) that dP(i+1) waits for.  Q_i is released after dK(i), dO_i after dV(i).
+      // dQ(i) that dP(i+1) waits for.  Every MMA waits for the copies of its own operands (dV(i+1)
+      // for dO(i+1), although P(i+1) alone is what it follows), and a stage is released only after
+      // the last MMA that reads it: Q_i after dK(i), dO_i after the later of dP(i) and dV(i).
       // descriptors of each operand buffer; a k-step adds its byte offset to the start address
       const uint64_t desc_k = sdesc_sw128(kb, 16384, 1024), desc_v = sdesc_sw128(vb, 16384, 1024);
       const uint64_t desc_ds = sdesc_sw128(dsb, 16384, 1024);
