@@ -3,7 +3,7 @@
 Only argument marshalling happens here (torch tensors -> device pointers, the current CUDA
 stream, output/workspace allocation through torch's caching allocator).  Every step of the
 computation runs in the library's CUDA kernels; there is no fallback of any kind: if the
-library is missing or the device is not an sm_100-family GPU the call raises.
+library is missing or the device is not an sm_103 GPU (GB300) the call raises.
 """
 
 from __future__ import annotations

@@ -105,12 +105,15 @@ float resolve_scale(float scale, int d) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// The kernels are built for sm_103a only (compute capability 10.3); on any other GPU no image
+// would load, so the call is refused before any launch.
 fa_status check_device() {
-  int dev = 0, major = 0;
+  int dev = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return FA_ERR_CUDA;
-  return (major == 10) ? FA_OK : FA_ERR_UNSUPPORTED;
+  return (major == 10 && minor == 3) ? FA_OK : FA_ERR_UNSUPPORTED;
 }
 
 fa_status check_workspace(void* ws, size_t bytes, size_t need) {
@@ -453,15 +456,9 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int d,
                  int causal, float scale, const int32_t* kv_lens, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  fa_status st = check_sizes(B, H, N, d);
-  if (st != FA_OK) return st;
-  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
-  st = fa_bwd_preprocess(O, dO, LSE, B, H, N, d, workspace, workspace_bytes, stream);
-  if (st != FA_OK) return st;
-  st = fa_bwd_dkdv(Q, K, V, dO, dK, dV, B, H, N, d, causal, scale, kv_lens, workspace,
-                   workspace_bytes, stream);
-  if (st != FA_OK) return st;
-  return fa_bwd_dq_convert(dQ, B, H, N, d, scale, workspace, workspace_bytes, stream);
+  // every argument is checked before the first of the three launches
+  return bwd_impl(dense_problem(B, H, H, N, d, causal, scale, kv_lens), Q, K, V, O, dO, LSE, dQ,
+                  dK, dV, workspace, workspace_bytes, /*deterministic=*/false, stream);
 }
 
 fa_status fa_bwd_deterministic(const void* Q, const void* K, const void* V, const void* O,

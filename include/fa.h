@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, non-positive size, bad workspace size */
-  FA_ERR_UNSUPPORTED = 2,  /* head dimension other than 64/128, no sm_100-family GPU */
+  FA_ERR_UNSUPPORTED = 2,  /* head dimension other than 64/128, or the GPU is not sm_103 */
   FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call or a kernel launch failed */
   FA_ERR_TIMEOUT = 4,      /* a device pipeline wait ran past its limit (see fa_get_error) */
   FA_ERR_WORKSPACE = 5     /* workspace pointer NULL or smaller than fa_bwd_workspace_size() */
@@ -71,8 +71,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 /*
  * Backward pass: dQ, dK, dV (all [B,H,N,d] bf16 outputs) of L with dL/dO = dO, given the
  * forward inputs Q, K, V, its outputs O and LSE, and the same B, H, N, d, causal, scale and
- * kv_lens.  Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert in that order on
- * `stream`.  workspace: DEVICE memory of at least fa_bwd_workspace_size() bytes, 256-byte
+ * kv_lens.  Checks every argument, then runs the work of fa_bwd_preprocess, fa_bwd_dkdv and
+ * fa_bwd_dq_convert in that order on `stream` (nothing is launched when a check fails).
+ * workspace: DEVICE memory of at least fa_bwd_workspace_size() bytes, 256-byte
  * aligned, owned by the caller, contents on entry irrelevant.
  * Cite: first page, 关键设计三 (recomputation of S_ij, P_ij from the saved statistic;
  * dV += P^T dO, dQ += dS K, dK += dS^T Q).
