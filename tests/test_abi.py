@@ -71,6 +71,13 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert lib.fa_bwd(*args, null, 1 << 20, null) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd(*args, p, 16, null) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd_dq_convert(p, 1, 1, 8, 64, -1.0, null, 0, null) == fa.FA_ERR_WORKSPACE
+    # fa_bwd checks every 16-byte operand pointer (Q, K, V, O, dO, dQ, dK, dV; LSE needs only
+    # 4 bytes) before its first launch, and before looking for a device
+    for bad in (0, 1, 2, 3, 4, 6, 7, 8):
+        bargs = [p] * 9
+        bargs[bad] = mis
+        rc = lib.fa_bwd(*bargs, 1, 1, 8, 64, 0, -1.0, null, p, 1 << 20, null)
+        assert rc == fa.FA_ERR_INVALID_ARG, (bad, rc)
 
 
 def test_binding_fails_loudly_without_library(tmp_path):
