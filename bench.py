@@ -389,6 +389,26 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def host_link_gbs(h_in, h_out, stream, reps=3):
+    """Plain copy rates of the host link just before the end-to-end run: `h_in` (pinned) to a
+    device buffer and back into `h_out` (pinned, same size), one direction at a time.  A slow
+    end-to-end figure with normal rates here is the pipeline's; with low rates, the link's."""
+    dbuf = torch.empty(h_in.shape, dtype=h_in.dtype, device=stream.device)
+    rates = {}
+    for name, copy in (("h2d", lambda: dbuf.copy_(h_in, non_blocking=True)),
+                       ("d2h", lambda: h_out.copy_(dbuf, non_blocking=True))):
+        copy()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            copy()
+        b.record(stream)
+        b.synchronize()
+        rates[name] = reps * h_in.numel() * h_in.element_size() / (a.elapsed_time(b) * 1e6)
+    del dbuf
+    return rates
+
+
 # ------------------------------------------------------------------------------- arms
 def workload_config(w, extra, args, world, l2):
     """The line's `config`: the workload's name and shape; `extra` is kv_lens (dense, may be
@@ -587,6 +607,7 @@ def run_ours(args, w, world, rank, local):
 
         for _ in range(2):
             e2e_step()
+        link = host_link_gbs(hq, hout["O"], stream)
         barrier(world)
         torch.cuda.synchronize()
         a, bv = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -599,7 +620,7 @@ def run_ours(args, w, world, rank, local):
         e2e_ms = max_over_ranks(a.elapsed_time(bv), world) / args.steps
         e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "chunks": len(ha.plan)}
+               "chunks": len(ha.plan), "host_link_gbs": link}
         assert fa.fa_get_error() == fa.FA_OK
 
     if rank != 0:
