@@ -93,8 +93,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 fa_status check_sizes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  // 128-row tiles of every (b, h) must be addressable with 32-bit coordinates
+  // 128-row tiles of every (b, h) must be addressable with 32-bit coordinates, and one block per
+  // (b, h, 128-row tile) must fit a 1-D grid (at most 2^31 - 1 blocks)
   if (N > (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>((N + 127) / 128) * B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -152,6 +154,7 @@ fa_status check_problem(const Problem& p) {
     if (p.total < 0 || p.kv_lens != nullptr || p.blk != nullptr) return FA_ERR_INVALID_ARG;
     if (static_cast<long long>(p.total) + 128LL * (p.B + 1) > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if (static_cast<long long>(p.H) * p.ws_tiles() * 128 > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    // (N here is the longest sequence; check_sizes bounded its tiles x B x H)
   }
   if (p.blk != nullptr && p.Hkv != p.H) return FA_ERR_INVALID_ARG;
   return FA_OK;

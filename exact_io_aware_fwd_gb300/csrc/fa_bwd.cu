@@ -108,7 +108,8 @@ struct TileRows {
 };
 
 // ------------------------------------------------------------------------------------------
-// Preprocess: grid (query tiles, B*H), 256 threads.
+// Preprocess: one block per (head slice, query tile), tph tiles per head slice, query tile
+// fastest (a 1-D grid: B*H may exceed the 65,535 limit of a grid's y dimension); 256 threads.
 template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16* __restrict__ O,
                                                              const __nv_bfloat16* __restrict__ dO,
@@ -116,11 +117,11 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              int nqt, float* __restrict__ neg_lse2,
                                                              float* __restrict__ neg_delta,
                                                              float* __restrict__ dq_acc,
-                                                             int zero_acc, RowGeo geo) {
+                                                             int zero_acc, int tph, RowGeo geo) {
   constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
   constexpr int RPW = 32 / G;  // rows per warp per pass
-  const int i = blockIdx.x;
-  const TileRows<kVarlen> tr(i, blockIdx.y, N, nqt, geo);
+  const int i = static_cast<int>(blockIdx.x % tph);
+  const TileRows<kVarlen> tr(i, static_cast<int>(blockIdx.x / tph), N, nqt, geo);
   if (kVarlen && i * 128 >= tr.n) return;  // past this sequence's end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane / G, cl = lane % G;
@@ -156,13 +157,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
 }
 
 // ------------------------------------------------------------------------------------------
-// dQ convert: grid (query tiles, B*H), 256 threads; thread = (row r, pair of column groups).
+// dQ convert: the preprocess kernel's 1-D grid, 256 threads; thread = (row r, pair of column
+// groups).
 template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
                                                              __nv_bfloat16* __restrict__ dQ, int N,
-                                                             int nqt, float scale, RowGeo geo) {
-  const int i = blockIdx.x;
-  const TileRows<kVarlen> tr(i, blockIdx.y, N, nqt, geo);
+                                                             int nqt, float scale, int tph,
+                                                             RowGeo geo) {
+  const int i = static_cast<int>(blockIdx.x % tph);
+  const TileRows<kVarlen> tr(i, static_cast<int>(blockIdx.x / tph), N, nqt, geo);
   const int r = threadIdx.x & 127;
   const int q = i * 128 + r;
   if (q >= tr.n) return;
@@ -731,21 +734,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 }  // namespace
 
+namespace {
+// Blocks of a 1-D grid of `tiles` per head slice times `heads` slices; 0 when that exceeds the
+// grid's x limit (2^31 - 1) or is empty.
+unsigned flat_grid(long long tiles, long long heads) {
+  const long long n = tiles * heads;
+  return (tiles <= 0 || heads <= 0 || n > 0x7fffffffLL) ? 0u : static_cast<unsigned>(n);
+}
+}  // namespace
+
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse, int BH,
                                   int N, float* neg_lse2, float* neg_delta, float* dq_acc,
                                   bool zero_acc, cudaStream_t s) {
   const int nqt = (N + 127) / 128;
-  const dim3 grid(nqt, BH);
+  const unsigned grid = flat_grid(nqt, BH);
+  if (grid == 0) return cudaErrorInvalidConfiguration;
   auto o = static_cast<const __nv_bfloat16*>(O);
   auto g = static_cast<const __nv_bfloat16*>(dO);
   const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
     bwd_preprocess_kernel<64, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta,
-                                                           dq_acc, zero_acc ? 1 : 0, geo);
+                                                           dq_acc, zero_acc ? 1 : 0, nqt, geo);
   else
     bwd_preprocess_kernel<128, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2,
                                                             neg_delta, dq_acc, zero_acc ? 1 : 0,
-                                                            geo);
+                                                            nqt, geo);
   return cudaGetLastError();
 }
 
@@ -754,42 +767,47 @@ cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, c
                                          int total, int ws_tiles, float* neg_lse2,
                                          float* neg_delta, float* dq_acc, bool zero_acc,
                                          cudaStream_t s) {
-  const dim3 grid(max_tiles, B * H);
+  const unsigned grid = flat_grid(max_tiles, static_cast<long long>(B) * H);
+  if (grid == 0) return cudaErrorInvalidConfiguration;
   auto o = static_cast<const __nv_bfloat16*>(O);
   auto g = static_cast<const __nv_bfloat16*>(dO);
   const RowGeo geo{cu, H, total, ws_tiles};
   if (d == 64)
     bwd_preprocess_kernel<64, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
-                                                          dq_acc, zero_acc ? 1 : 0, geo);
+                                                          dq_acc, zero_acc ? 1 : 0, max_tiles, geo);
   else
     bwd_preprocess_kernel<128, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
-                                                           dq_acc, zero_acc ? 1 : 0, geo);
+                                                           dq_acc, zero_acc ? 1 : 0, max_tiles,
+                                                           geo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N, float scale,
                                   cudaStream_t s) {
   const int nqt = (N + 127) / 128;
-  const dim3 grid(nqt, BH);
+  const unsigned grid = flat_grid(nqt, BH);
+  if (grid == 0) return cudaErrorInvalidConfiguration;
   auto out = static_cast<__nv_bfloat16*>(dQ);
   const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
-    bwd_dq_convert_kernel<64, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, geo);
+    bwd_dq_convert_kernel<64, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, nqt, geo);
   else
-    bwd_dq_convert_kernel<128, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, geo);
+    bwd_dq_convert_kernel<128, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, nqt, geo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, void* dQ, const int32_t* cu,
                                          int B, int H, int max_tiles, int total, int ws_tiles,
                                          float scale, cudaStream_t s) {
-  const dim3 grid(max_tiles, B * H);
+  const unsigned grid = flat_grid(max_tiles, static_cast<long long>(B) * H);
+  if (grid == 0) return cudaErrorInvalidConfiguration;
   auto out = static_cast<__nv_bfloat16*>(dQ);
   const RowGeo geo{cu, H, total, ws_tiles};
   if (d == 64)
-    bwd_dq_convert_kernel<64, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, geo);
+    bwd_dq_convert_kernel<64, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, max_tiles, geo);
   else
-    bwd_dq_convert_kernel<128, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, geo);
+    bwd_dq_convert_kernel<128, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, max_tiles,
+                                                           geo);
   return cudaGetLastError();
 }
 

@@ -167,3 +167,15 @@ def test_host_pipeline_graph_replays(causal, kvr):
         rel = torch.linalg.norm(got["dQ"].double() - ref["dQ"].cpu().double()) / torch.linalg.norm(
             ref["dQ"].cpu().double())
         assert rel < 1e-2
+
+
+@pytest.mark.parametrize("causal,det", [(False, False), (True, False), (True, True)])
+def test_more_head_slices_than_a_grid_row(causal, det):
+    """B * H = 70,000 head slices (more than the 65,535 blocks a grid's y dimension allows): every
+    kernel of the path takes its head slice from a 1-D block index, so the last slices are
+    computed like the first."""
+    B, H, N, d = 35000, 2, 10, 64
+    q, k, v, do, _ = make_inputs(B, H, N, d, seed=70000)
+    slices = [(0, 0), (32767, 1), (32768, 0), (B - 1, 1)]
+    check_case(q, k, v, do, causal, None, None, slices=slices, label=f"B*H={B * H}",
+               deterministic=det)
