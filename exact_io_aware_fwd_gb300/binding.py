@@ -138,7 +138,36 @@ def _check_qkv(*ts):
             raise ValueError("expected contiguous CUDA bfloat16 tensors")
         if t.shape != ref.shape:
             raise ValueError("shape mismatch")
+        if t.device != ref.device:
+            raise ValueError("tensors on different devices")
     return tuple(ref.shape)
+
+
+def _want(t, shape, dtype, device, name):
+    """`t` itself after checking that the library may write or read it as a dense array of
+    `shape`: a contiguous `dtype` tensor on `device` (the kernels address it by pointer only)."""
+    if (not isinstance(t, torch.Tensor) or t.device != device or t.dtype != dtype
+            or not t.is_contiguous() or tuple(t.shape) != tuple(shape)):
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} "
+                         f"on {device}")
+    return t
+
+
+def _out(t, shape, dtype, device, name):
+    """A new output tensor, or the caller's after the checks of `_want`."""
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _want(t, shape, dtype, device, name)
+
+
+def _workspace(ws, nbytes, device):
+    """(tensor, size in bytes) of the backward workspace: a new byte array, or the caller's
+    contiguous tensor on `device` (any dtype; its size is counted in bytes)."""
+    if ws is None:
+        return torch.empty(max(int(nbytes), 1), dtype=torch.uint8, device=device), max(int(nbytes), 1)
+    if not isinstance(ws, torch.Tensor) or ws.device != device or not ws.is_contiguous():
+        raise ValueError(f"workspace must be a contiguous tensor on {device}")
+    return ws, ws.numel() * ws.element_size()
 
 
 def _kv(kv_lens, B, device):
@@ -157,9 +186,8 @@ def _scale(scale):
 def fa_fwd(q, k, v, causal=False, scale=None, kv_lens=None, out=None, lse=None, stream=None):
     """O, LSE = exact attention of [B,H,N,d] bf16 q, k, v (see include/fa.h)."""
     B, H, N, d = _check_qkv(q, k, v)
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32) if lse is None else lse
-    _check_qkv(q, out)
+    out = _out(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, N), torch.float32, q.device, "lse")
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
                                int(bool(causal)), _scale(scale), _ptr(kv), _stream(stream))
@@ -184,14 +212,14 @@ def fa_bwd(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dq=None,
            dv=None, workspace=None, stream=None):
     """dQ, dK, dV of exact attention given the forward's O and LSE (see include/fa.h)."""
     B, H, N, d = _check_qkv(q, k, v, o, do)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    ws = workspace_for(q) if workspace is None else workspace
+    _want(lse, (B, H, N), torch.float32, q.device, "lse")
+    dq, dk, dv = (_out(t, q.shape, torch.bfloat16, q.device, n)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
+    ws, ws_bytes = _workspace(workspace, fa_bwd_workspace_size(B, H, N, d), q.device)
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                                _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), _scale(scale),
-                               _ptr(kv), _ptr(ws), ws.numel(), _stream(stream))
+                               _ptr(kv), _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "fa_bwd")
     return dq, dk, dv
 
@@ -200,23 +228,25 @@ def fa_bwd_deterministic(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=
                          dk=None, dv=None, workspace=None, stream=None):
     """fa_bwd with run-to-run bit-identical results (dQ without atomics; see include/fa.h)."""
     B, H, N, d = _check_qkv(q, k, v, o, do)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    ws = workspace_for(q) if workspace is None else workspace
+    _want(lse, (B, H, N), torch.float32, q.device, "lse")
+    dq, dk, dv = (_out(t, q.shape, torch.bfloat16, q.device, n)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
+    ws, ws_bytes = _workspace(workspace, fa_bwd_workspace_size(B, H, N, d), q.device)
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
                                              _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
                                              int(bool(causal)), _scale(scale), _ptr(kv), _ptr(ws),
-                                             ws.numel(), _stream(stream))
+                                             ws_bytes, _stream(stream))
     _check(st, "fa_bwd_deterministic")
     return dq, dk, dv
 
 
 def fa_bwd_preprocess(o, do, lse, workspace, stream=None):
     B, H, N, d = _check_qkv(o, do)
+    _want(lse, (B, H, N), torch.float32, o.device, "lse")
+    ws, ws_bytes = _workspace(workspace, 0, o.device)
     st = load_library().fa_bwd_preprocess(_ptr(o), _ptr(do), _ptr(lse), B, H, N, d,
-                                          _ptr(workspace), workspace.numel(), _stream(stream))
+                                          _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "fa_bwd_preprocess")
 
 
@@ -224,16 +254,18 @@ def fa_bwd_dkdv(q, k, v, do, dk, dv, workspace, causal=False, scale=None, kv_len
                 stream=None):
     B, H, N, d = _check_qkv(q, k, v, do, dk, dv)
     kv = _kv(kv_lens, B, q.device)
+    ws, ws_bytes = _workspace(workspace, 0, q.device)
     st = load_library().fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dk), _ptr(dv), B,
                                     H, N, d, int(bool(causal)), _scale(scale), _ptr(kv),
-                                    _ptr(workspace), workspace.numel(), _stream(stream))
+                                    _ptr(ws), ws_bytes, _stream(stream))
     _check(st, "fa_bwd_dkdv")
 
 
 def fa_bwd_dq_convert(dq, workspace, scale=None, stream=None):
     B, H, N, d = _check_qkv(dq)
-    st = load_library().fa_bwd_dq_convert(_ptr(dq), B, H, N, d, _scale(scale), _ptr(workspace),
-                                          workspace.numel(), _stream(stream))
+    ws, ws_bytes = _workspace(workspace, 0, dq.device)
+    st = load_library().fa_bwd_dq_convert(_ptr(dq), B, H, N, d, _scale(scale), _ptr(ws),
+                                          ws_bytes, _stream(stream))
     _check(st, "fa_bwd_dq_convert")
 
 
@@ -242,9 +274,9 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, 
     """fa_bwd with the library's static workspace, for callers that cannot allocate device
     memory (see include/fa.h); calls that overlap on the GPU must be serialised."""
     B, H, N, d = _check_qkv(q, k, v, o, do)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    _want(lse, (B, H, N), torch.float32, q.device, "lse")
+    dq, dk, dv = (_out(t, q.shape, torch.bfloat16, q.device, n)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                        _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
@@ -299,8 +331,10 @@ def fa_fwd_block_sparse(q, k, v, index: BlockIndex, causal=False, scale=None, kv
     B, H, N, d = _check_qkv(q, k, v)
     if index.N != N:
         raise ValueError("block index built for another N")
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    if index.tensor.device != q.device:
+        raise ValueError("block index on another device")
+    out = _out(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, N), torch.float32, q.device, "lse")
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H,
                                             N, d, int(bool(causal)), _scale(scale), _ptr(kv),
@@ -316,16 +350,18 @@ def fa_bwd_block_sparse(q, k, v, o, do, lse, index: BlockIndex, causal=False, sc
     B, H, N, d = _check_qkv(q, k, v, o, do)
     if index.N != N:
         raise ValueError("block index built for another N")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    ws = workspace_for(q) if workspace is None else workspace
+    if index.tensor.device != q.device:
+        raise ValueError("block index on another device")
+    _want(lse, (B, H, N), torch.float32, q.device, "lse")
+    dq, dk, dv = (_out(t, q.shape, torch.bfloat16, q.device, n)
+                  for t, n in ((dq, "dq"), (dk, "dk"), (dv, "dv")))
+    ws, ws_bytes = _workspace(workspace, fa_bwd_workspace_size(B, H, N, d), q.device)
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_bwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do),
                                             _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
                                             int(bool(causal)), _scale(scale), _ptr(kv),
                                             _ptr(index.tensor), index.mask_heads,
-                                            int(bool(deterministic)), _ptr(ws), ws.numel(),
+                                            int(bool(deterministic)), _ptr(ws), ws_bytes,
                                             _stream(stream))
     _check(st, "fa_bwd_block_sparse")
     return dq, dk, dv
@@ -339,16 +375,17 @@ def _check_group(q, k):
     B, H, N, d = q.shape
     if k.shape[0] != B or k.shape[2:] != (N, d) or H % k.shape[1] != 0:
         raise ValueError("K must be [B, Hkv, N, d] with H % Hkv == 0")
+    if k.device != q.device:
+        raise ValueError("tensors on different devices")
     return B, H, k.shape[1], N, d
 
 
 def fa_fwd_gqa(q, k, v, causal=False, scale=None, kv_lens=None, out=None, lse=None, stream=None):
     """Grouped-query forward: q [B, H, N, d], k and v [B, Hkv, N, d] (see include/fa.h)."""
     B, H, Hkv, N, d = _check_group(q, k)
-    if v.shape != k.shape:
-        raise ValueError("V must have K's shape")
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _want(v, k.shape, torch.bfloat16, q.device, "v")
+    out = _out(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out(lse, (B, H, N), torch.float32, q.device, "lse")
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, N,
                                    d, int(bool(causal)), _scale(scale), _ptr(kv), _stream(stream))
@@ -360,15 +397,19 @@ def fa_bwd_gqa(q, k, v, o, do, lse, causal=False, scale=None, kv_lens=None, dete
                dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Grouped-query backward; dK, dV [B, Hkv, N, d] sum over each key/value head's group."""
     B, H, Hkv, N, d = _check_group(q, k)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    ws = workspace_for(q) if workspace is None else workspace
+    _want(v, k.shape, torch.bfloat16, q.device, "v")
+    _want(o, q.shape, torch.bfloat16, q.device, "o")
+    _want(do, q.shape, torch.bfloat16, q.device, "do")
+    _want(lse, (B, H, N), torch.float32, q.device, "lse")
+    dq = _out(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out(dv, k.shape, torch.bfloat16, q.device, "dv")
+    ws, ws_bytes = _workspace(workspace, fa_bwd_workspace_size(B, H, N, d), q.device)
     kv = _kv(kv_lens, B, q.device)
     st = load_library().fa_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, N, d,
                                    int(bool(causal)), _scale(scale), _ptr(kv),
-                                   int(bool(deterministic)), _ptr(ws), ws.numel(),
+                                   int(bool(deterministic)), _ptr(ws), ws_bytes,
                                    _stream(stream))
     _check(st, "fa_bwd_gqa")
     return dq, dk, dv
@@ -381,8 +422,12 @@ def _check_packed(q, k, cu_seqlens):
     total, H, d = q.shape
     if k.shape[0] != total or k.shape[2] != d or H % k.shape[1] != 0:
         raise ValueError("K must be [total, Hkv, d] with H % Hkv == 0")
-    if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
-        raise ValueError("cu_seqlens must be a CUDA int32 vector of B + 1 offsets")
+    if (cu_seqlens.dtype != torch.int32 or cu_seqlens.device != q.device
+            or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2 or not cu_seqlens.is_contiguous()):
+        raise ValueError("cu_seqlens must be a contiguous int32 vector of B + 1 offsets on "
+                         "q's device")
+    if k.device != q.device:
+        raise ValueError("tensors on different devices")
     return total, H, k.shape[1], d, cu_seqlens.numel() - 1
 
 
@@ -394,8 +439,9 @@ def fa_fwd_varlen(q, k, v, cu_seqlens, max_seqlen, causal=False, scale=None, out
                   stream=None):
     """Packed variable-length forward: q [total, H, d], k and v [total, Hkv, d], LSE [H, total]."""
     total, H, Hkv, d, B = _check_packed(q, k, cu_seqlens)
-    out = torch.empty_like(q) if out is None else out
-    lse = torch.empty((H, total), dtype=torch.float32, device=q.device) if lse is None else lse
+    _want(v, k.shape, torch.bfloat16, q.device, "v")
+    out = _out(out, q.shape, torch.bfloat16, q.device, "out")
+    lse = _out(lse, (H, total), torch.float32, q.device, "lse")
     st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
                                       _ptr(cu_seqlens), B, int(max_seqlen), total, H, Hkv, d,
                                       int(bool(causal)), _scale(scale), _stream(stream))
@@ -407,17 +453,20 @@ def fa_bwd_varlen(q, k, v, o, do, lse, cu_seqlens, max_seqlen, causal=False, sca
                   deterministic=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Packed variable-length backward (see include/fa.h)."""
     total, H, Hkv, d, B = _check_packed(q, k, cu_seqlens)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if workspace is None:
-        workspace = torch.empty(max(fa_bwd_varlen_workspace_size(B, total, H, d), 1),
-                                dtype=torch.uint8, device=q.device)
+    _want(v, k.shape, torch.bfloat16, q.device, "v")
+    _want(o, q.shape, torch.bfloat16, q.device, "o")
+    _want(do, q.shape, torch.bfloat16, q.device, "do")
+    _want(lse, (H, total), torch.float32, q.device, "lse")
+    dq = _out(dq, q.shape, torch.bfloat16, q.device, "dq")
+    dk = _out(dk, k.shape, torch.bfloat16, q.device, "dk")
+    dv = _out(dv, k.shape, torch.bfloat16, q.device, "dv")
+    workspace, ws_bytes = _workspace(workspace, fa_bwd_varlen_workspace_size(B, total, H, d),
+                                     q.device)
     st = load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse),
                                       _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens), B,
                                       int(max_seqlen), total, H, Hkv, d, int(bool(causal)),
                                       _scale(scale), int(bool(deterministic)), _ptr(workspace),
-                                      workspace.numel(), _stream(stream))
+                                      ws_bytes, _stream(stream))
     _check(st, "fa_bwd_varlen")
     return dq, dk, dv
 
