@@ -17,7 +17,7 @@
  *     memory owned by the caller and must be 16-byte aligned.  The library allocates no
  *     device memory; the backward pass takes a caller-provided workspace.
  *   - d (head dimension) is 64 or 128; N >= 1 is any length (no tile multiple needed);
- *     B * H <= 2^31 - 1.
+ *     ceil(N / 128) * B * H <= 2^31 - 1 (one thread block per 128-row tile of every head).
  *   - scale < 0 selects the default 1/sqrt(d) (softmax_scale=None in the pages' interface,
  *     first page, section 使用契约); scale == 0 is allowed.
  *   - causal != 0 masks key j > query i.  kv_lens (DEVICE int32[B], or NULL for "all N") masks
