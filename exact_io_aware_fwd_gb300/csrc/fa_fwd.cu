@@ -15,6 +15,9 @@
 //  * warp 1: single-thread tcgen05.mma issuer.  S_t = Q_t K_j^T (both operands in smem) and
 //    O_t += P_t V_j with P_t read straight from tensor memory, alternating the two tiles so
 //    that one tile's softmax overlaps the other tile's MMAs (ping-pong of FlashAttention-3).
+//  * dense d = 64 (kHalfSteps): each 128-key K/V stage is consumed as two 64-key half steps,
+//    so the two tiles need 256 tensor-memory columns and two CTAs (of 320 threads, softmax in
+//    warps 2-9) share an SM: four query tiles in flight per SM.
 //  * warps 4-7 / 8-11: one warpgroup per query tile, one thread per query row: tcgen05.ld of
 //    the S row, row max, exp2 of (S * scale * log2 e - m), P packed to bf16 and stored back
 //    over S in tensor memory, row sum.  O~ is rescaled in tensor memory only when the running
@@ -85,10 +88,33 @@ __device__ __forceinline__ float2 exp2_poly2(float2 x) {
 }
 constexpr float kLn2 = 0.693147180559945309f;
 
-template <int D>
+// O += P V over 64 keys: A = bf16 pairs in tensor memory, 8 columns per 16-key step; B (V)
+// MN-major, 16 key rows of 128 bytes = +2048 bytes per step.
+__device__ __forceinline__ void mma_ts_k64_step4(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                                 uint32_t id, uint32_t accumulate) {
+  asm volatile(FA_MMA_HEAD
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+               FA_MMA_TS_STEP(8, 128) FA_MMA_TS_STEP(16, 256) FA_MMA_TS_STEP(24, 384) "}"
+               :: "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(accumulate), "n"(1) : "memory");
+}
+
+// Dense d = 64: each 128-key K/V stage is consumed as two 64-key half steps (S of 128 x 64,
+// softmax over 64 scores per row, P V over 64 keys), so a CTA's two query tiles need 64 + 64
+// tensor-memory columns each and two CTAs share an SM: four query tiles in flight per SM
+// instead of two.  At d = 64 the tiles' serial chains (S -> softmax -> P V), not the tensor
+// pipe, set the pace; more tiles in flight fill the pipe.
+template <int D, bool kSparse, bool kVarlen>
+constexpr bool kHalfSteps = (D == 64) && !kSparse && !kVarlen;
+// Threads per CTA: warp 0 TMA, warp 1 MMA, then two softmax warpgroups (warps 4-11; with half
+// steps warps 2-9, so that two CTAs' 640 threads get 96 registers each: a warp's tensor-memory
+// lanes follow warp % 4, so any four consecutive warps cover the 128 rows).
+template <int D, bool kSparse, bool kVarlen>
+constexpr int kFwdThreads = kHalfSteps<D, kSparse, kVarlen> ? 320 : 384;
+
+template <int D, bool kHalf = false>
 struct FwdLayout {
   static constexpr uint32_t kTile = 128u * D * 2u;  // one 128 x D bf16 tile
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kStages = kHalf ? 2 : ((D == 64) ? 4 : 2);
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + 2 * kTile;
   static constexpr uint32_t kV = kK + kStages * kTile;
@@ -99,9 +125,10 @@ struct FwdLayout {
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kCnt = kAbort + 4;  // block-sparse counts: positions, n_0, n_1
   static constexpr uint32_t kBytes = kCnt + 12;
-  // TMEM columns: S_0, S_1 (128 each), O_0, O_1 (D each)
-  static constexpr uint32_t kColS0 = 0, kColO0 = 256;
-  static constexpr uint32_t kTmemCols = 512;
+  // TMEM columns: S_0, S_1 (128 each, 64 with half steps), O_0, O_1 (D each)
+  static constexpr uint32_t kSCols = kHalf ? 64 : 128;
+  static constexpr uint32_t kColS0 = 0, kColO0 = 2 * kSCols;
+  static constexpr uint32_t kTmemCols = kHalf ? 256 : 512;
 };
 
 // Wait that ignores the abort flag (used only to drain this CTA's own asynchronous work
@@ -132,11 +159,13 @@ __device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, in
 }
 
 template <int D, bool kSparse, bool kVarlen>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
+                                  (kHalfSteps<D, kSparse, kVarlen> ? 2 : 1))
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                const FwdArgs a) {
-  using L = FwdLayout<D>;
+  constexpr bool kHalf = kHalfSteps<D, kSparse, kVarlen>;
+  using L = FwdLayout<D, kHalf>;
   constexpr int S = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -191,13 +220,14 @@ __global__ void __launch_bounds__(384, 1)
   const int kv_y0 = kVarlen ? hk : 0, kv_z0 = kVarlen ? seq_start : b * a.Hkv + hk;
   auto row_y = [&](int y0, int r) { return kVarlen ? y0 : r; };
   auto row_z = [&](int z0, int r) { return kVarlen ? z0 + r : z0; };
-  int nb[2];
+  int nb[2], nh[2];  // key tiles (128 keys) and half steps (64 keys) of each query tile
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt0 = q0 + 128 * t;
     int nkeys = kv_len;
     if (a.causal) nkeys = min(nkeys, qt0 + 128);
     nb[t] = (qt0 < N) ? (nkeys + 127) / 128 : 0;
+    nh[t] = (qt0 < N) ? (nkeys + 63) / 64 : 0;
   }
   const int nb_max = max(nb[0], nb[1]);
   const int T = (N + 127) / 128;
@@ -300,7 +330,54 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ================= MMA issuer
-    if (lane == 0 && npos > 0) {
+    if (kHalf && lane == 0 && npos > 0) {
+      // Half steps hs = 0 .. nh_max: step hs reads half (hs & 1) of K/V stage hs >> 1.  Per
+      // step and query tile: P V of the previous half step, then S of this one (S overwrites
+      // that tile's P).  A K stage is released after the S MMAs of its last half step, a V
+      // stage after the P V MMAs of its last half step.
+      constexpr uint32_t idSh = idesc_bf16(128, 64, false, false);  // S half: 64 keys
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);     // O += P V, V is MN-major
+      constexpr uint32_t kHalfBytes = 64u * 128u;                   // 64 key rows of 128 bytes
+      bool ok = mbar_wait(q_full, 0, ctl);
+      const int nhmax = max(nh[0], nh[1]);
+      int cnt[2] = {0, 0};  // S MMAs issued per query tile
+      for (int hs = 0; ok && hs <= nhmax; ++hs) {
+        const int j = hs >> 1, hf = hs & 1;  // stage position and half of this step
+        const int s = j % S;
+        const int jp = (hs - 1) >> 1, hp = (hs - 1) & 1;  // those of the previous step (hs >= 1)
+        const int sp = (hs >= 1) ? jp % S : 0;
+        if (hs < nhmax && hf == 0 && !(ok = mbar_wait(&k_full[s], (j / S) & 1, ctl))) break;
+        if (hs >= 1 && hp == 0 && !(ok = mbar_wait(&v_full[sp], (jp / S) & 1, ctl))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (hs >= 1 && hs - 1 < nh[t]) {
+            if (!(ok = mbar_wait(&p_full[t], (cnt[t] - 1) & 1, ctl))) break;
+            tc_fence_after();
+            mma_ts_k64_step4(tmem + L::kColO0 + D * t, tmem + L::kColS0 + L::kSCols * t,
+                             sdesc_sw128(sbase + L::kV + sp * L::kTile + hp * kHalfBytes, 16384,
+                                         1024),
+                             idO, cnt[t] > 1 ? 1u : 0u);
+            if (cnt[t] == nh[t]) mma_commit(&o_full[t]);  // the tile's last P V
+          }
+          if (hs < nh[t]) {
+            mma_ss_kmajor<D>(tmem + L::kColS0 + L::kSCols * t,
+                             sdesc_sw128(sbase + L::kQ + t * L::kTile, 16384, 1024),
+                             sdesc_sw128(sbase + L::kK + s * L::kTile + hf * kHalfBytes, 16384,
+                                         1024),
+                             idSh, 0u);
+            mma_commit(&s_full[t]);
+            ++cnt[t];
+          }
+        }
+        if (!ok) break;
+        if (hs < nhmax && (hf == 1 || hs == nhmax - 1)) mma_commit(&k_empty[s]);
+        if (hs >= 1 && (hp == 1 || hs - 1 == nhmax - 1)) mma_commit(&v_empty[sp]);
+      }
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0, ctl);
+    }
+    if (!kHalf && lane == 0 && npos > 0) {
       constexpr uint32_t idS = idesc_bf16(128, 128, false, false);  // S = Q K^T, both K-major
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);     // O += P V, V is MN-major
       bool ok = mbar_wait(q_full, 0, ctl);
@@ -362,24 +439,124 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(mma_done);
       drain_wait(mma_done, 0, ctl);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= (kHalf ? 2u : 4u)) {
     // ================= softmax warpgroups: one per query tile, one thread per query row
-    const int t = (warp - 4) >> 2;
+    const int t = (warp - (kHalf ? 2 : 4)) >> 2;
     const uint32_t quad = warp & 3;
     const int row = quad * 32 + lane;
     const int qt0 = q0 + 128 * t;
     const int qi = qt0 + row;
     const uint32_t lanes = (quad * 32u) << 16;
-    const uint32_t tS = tmem + lanes + L::kColS0 + 128 * t;
+    const uint32_t tS = tmem + lanes + L::kColS0 + L::kSCols * t;
     const uint32_t tO = tmem + lanes + L::kColO0 + D * t;
     const float c2 = a.scale_log2;
-    const int n = ncnt[t];
+    const int n = kHalf ? nh[t] : ncnt[t];
     int kt_next = (kSparse && n > 0) ? __ldg(r_list[t]) : 0;
     float m_run = -INFINITY;  // running max of scale*log2(e)*s (log2 units)
     float l_run = 0.f;        // running sum of exp2(. - m_run)
     float lr_run = 0.f;       // the same sum over the bf16-rounded values (normalises O~)
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
+    if constexpr (kHalf) {
+      // one 64-key half step per S: the same online softmax over 64 scores per row
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = mbar_wait_warp(&s_full[t], j & 1, ctl))) break;
+        tc_fence_after();
+        uint32_t s[64];
+        tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+        tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+        tmem_wait_ld();
+        reg_fence(s);
+        const int k0 = j * 64;
+        const bool masked = (k0 + 64 > kv_len) || (a.causal && k0 + 64 > qt0);
+        const int klim = a.causal ? min(kv_len, qi + 1) : kv_len;  // keys < klim are visible
+        float mxv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (k0 + c < klim) mxv[c & 3] = fmaxf(mxv[c & 3], __uint_as_float(s[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            mxv[0] = max3(mxv[0], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+            mxv[1] = max3(mxv[1], __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+            mxv[2] = max3(mxv[2], __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+            mxv[3] = max3(mxv[3], __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+          }
+        }
+        const float mx = fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3]));
+        const float m_tile = mx * c2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_tile > m_run + kRescaleThreshold) {
+          rescale = true;
+          alpha = ex2(m_run - m_tile);  // 0 on the first step (m_run = -inf)
+          l_run *= alpha;
+          lr_run *= alpha;
+          m_run = m_tile;
+        }
+        const float2 cc = make_float2(c2, c2);
+        const float2 nm = make_float2(-m_run, -m_run);
+        float2 sumv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float sum_r = 0.f;
+        uint32_t p[32];
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(
+                make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), cc, nm);
+            const float x0 = (k0 + 2 * c < klim) ? ex2(x.x) : 0.f;
+            const float x1 = (k0 + 2 * c + 1 < klim) ? ex2(x.y) : 0.f;
+            p[c] = pack_bf16(x0, x1);
+            sumv[c & 1] = add2(sumv[c & 1], make_float2(x0, x1));
+            if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 x = fma2(
+                make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])), cc, nm);
+            float x0, x1;
+            if (FA_SOFT_EXP2 > 0 && c % (FA_SOFT_EXP2 > 0 ? FA_SOFT_EXP2 : 1) == FA_SOFT_EXP2 - 1) {
+              const float2 e = exp2_poly2(x);
+              x0 = e.x;
+              x1 = e.y;
+            } else {
+              x0 = ex2(x.x);
+              x1 = ex2(x.y);
+            }
+            p[c] = pack_bf16(x0, x1);
+            sumv[c & 1] = add2(sumv[c & 1], make_float2(x0, x1));
+            if (FA_ROUNDED_SUM) sum_r += bf16_lo(p[c]) + bf16_hi(p[c]);
+          }
+        }
+        l_run += (sumv[0].x + sumv[1].x) + (sumv[0].y + sumv[1].y);
+        lr_run += sum_r;
+        tmem_st32(tS + 0, p);  // P over the first 32 columns of this tile's S
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + 32 * c, o);
+            tmem_wait_ld();
+            reg_fence(o);
+            const float2 aa = make_float2(alpha, alpha);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 v = mul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])),
+                                    aa);
+              o[e] = __float_as_uint(v.x);
+              o[e + 1] = __float_as_uint(v.y);
+            }
+            tmem_st32(tO + 32 * c, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[t]);
+      }
+    }
+    for (int j = 0; !kHalf && j < n; ++j) {
       const int kt = kSparse ? kt_next : j;  // key tile of this query tile's j-th S
       if (kSparse && j + 1 < n) kt_next = __ldg(r_list[t] + j + 1);
       if (!(ok = mbar_wait_warp(&s_full[t], j & 1, ctl))) break;
@@ -566,13 +743,14 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, bool kSparse, bool kVarlen>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, FwdArgs a, cudaStream_t st) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, kHalfSteps<D, kSparse, kVarlen>>;
   const uint32_t smem = L::kBytes + 1024;
   cudaError_t e = ensure_smem_limit<fwd_kernel<D, kSparse, kVarlen>>(smem);
   if (e != cudaSuccess) return e;
   a.smem_bytes = smem;
   const unsigned grid = static_cast<unsigned>(a.num_qblocks) * static_cast<unsigned>(a.BH);
-  fwd_kernel<D, kSparse, kVarlen><<<grid, 384, smem, st>>>(tq, tk, tv, to, a);
+  fwd_kernel<D, kSparse, kVarlen><<<grid, kFwdThreads<D, kSparse, kVarlen>, smem, st>>>(tq, tk,
+                                                                                       tv, to, a);
   return cudaGetLastError();
 }
 

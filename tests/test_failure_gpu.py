@@ -23,6 +23,12 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    fa.build()
+    fa.load_library()
+
+
 @pytest.fixture(scope="module")
 def selftest_lib(tmp_path_factory):
     out = tmp_path_factory.mktemp("selftest") / "libwait_selftest.so"
