@@ -457,7 +457,8 @@ __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
     float lr_run = 0.f;       // the same sum over the bf16-rounded values (normalises O~)
     bool ok = true;
     if constexpr (kHalf) {
-      // one 64-key half step per S: the same online softmax over 64 scores per row
+      // one 64-key half step per S: the same online softmax over 64 scores per row (a loop of
+      // its own, so that the 128-key loop below, which the d = 128 kernels run, is untouched)
       for (int j = 0; j < n; ++j) {
         if (!(ok = mbar_wait_warp(&s_full[t], j & 1, ctl))) break;
         tc_fence_after();
