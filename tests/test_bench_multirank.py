@@ -22,7 +22,12 @@ def test_reference_arm_two_ranks_gloo():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["full_step_seconds_extrapolated"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas x2"
+    # the same config keys as the CUDA arm's line
+    assert set(d["config"]) == {"workload", "B", "H", "N", "d", "causal", "kv_lens", "l2",
+                                "parallelism", "bwd", "block_mask", "Hkv", "seqlens"}
 
 
 def test_max_over_ranks_gloo(tmp_path):
