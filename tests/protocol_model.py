@@ -1,0 +1,470 @@
+"""Model checker for the kernels' mbarrier pipelines (test infrastructure, CPU only).
+
+The CUDA kernels split each CTA into roles — a TMA producer, one MMA-issuing thread, warps that
+compute the softmax (forward) or P and dS (backward) — which hand shared-memory stages and
+tensor-memory regions to one another through mbarriers.  compute-sanitizer is not available
+where the kernels run, and a protocol error (a wait on the wrong phase, a stage released before
+its last reader, an MMA issued before its operand's copy has landed) shows up on the GPU only
+intermittently.  This module restates each kernel's control flow — its waits, arrivals, commits,
+and which buffer each step reads or writes — as Python generators, and runs them under random
+interleavings:
+
+* an mbarrier completes a phase when its expected arrivals have come in; a wait on parity P
+  passes while the current phase's parity differs from P (the hardware's try_wait.parity), and
+  the checker asserts that the phase it passed on is the one the waiter meant (a waiter two or
+  more phases behind would pass on the wrong phase);
+* copies and MMAs take effect when issued, and a commit arrives at once (every earlier MMA of the
+  thread has then completed), which keeps the order the hardware guarantees;
+* every buffer (a K/V/Q/dO stage, a tensor-memory region per 32-lane quadrant, the dS staging
+  buffer) records what it holds and whether a reader still needs its contents; a read asserts
+  the expected content, and an overwrite asserts that no reader is pending.
+
+A missing wait lets some interleaving read a stage before its copy lands; a release before the
+last reader lets the producer overwrite a stage that is still needed; both fail here.  The models
+follow the kernels' code (fa_fwd.cu: fwd_kernel's producer, MMA issuer and softmax warpgroups,
+dense and half-step; fa_bwd.cu: bwd_dkdv_kernel's producer, MMA issuer and elementwise
+warpgroups) and must change with it.
+"""
+
+from __future__ import annotations
+
+import random
+
+
+class Bar:
+    def __init__(self, count, name):
+        self.count, self.pending, self.c, self.name = count, count, 0, name
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0, self.name
+        if self.pending == 0:
+            self.c += 1
+            self.pending = self.count
+
+    def try_wait(self, parity):
+        return (self.c & 1) != parity
+
+
+class Buf:
+    """A buffer: what it holds and the readers that still need it."""
+
+    def __init__(self, name):
+        self.name, self.val, self.readers = name, None, 0
+
+    def write(self, val, readers=0):
+        assert self.readers == 0, f"{self.name}: overwritten ({self.val} -> {val}) with a reader pending"
+        self.val, self.readers = val, readers
+
+    def read(self, expect, consume=False):
+        assert self.val == expect, f"{self.name}: read {self.val}, expected {expect}"
+        if consume:
+            assert self.readers > 0, f"{self.name}: consumed twice"
+            self.readers -= 1
+
+
+def wait(bar, parity, completed):
+    """Generator: spin until the barrier passes `parity`; then the completed phases must number
+    exactly `completed` (the phase the waiter means)."""
+    while not bar.try_wait(parity):
+        yield
+    assert bar.c == completed, f"{bar.name}: passed with {bar.c} completed phases, meant {completed}"
+
+
+class Sim:
+    """Random interleaving of agents (generators), with the two asynchronous engines of the
+    hardware: the tensor pipe, which runs the MMA thread's operations (and commits) in issue
+    order at times of its own, and the copy engine, whose copies each land at a time of their
+    own."""
+
+    def __init__(self, seed):
+        import random
+
+        self.rng = random.Random(seed)
+        self.live = []
+        self.queue = []          # tensor pipe: operations in issue order
+        self.issuer_done = False
+
+    def spawn(self, gen):
+        self.live.append(gen)
+
+    def copy(self, fn):
+        """An asynchronous copy: `fn` (write the stage, arrive on its barrier) runs after a random
+        delay, long enough for the consumers to race ahead of it."""
+        delay = self.rng.randint(0, 40)
+
+        def agent():
+            for _ in range(delay + 1):
+                yield
+            fn()
+        self.spawn(agent())
+
+    def issue(self, fn):
+        """An MMA or commit: `fn` runs when the tensor pipe reaches it."""
+        self.queue.append(fn)
+
+    def _pipe(self):
+        while not (self.issuer_done and not self.queue):
+            if self.queue:
+                self.queue.pop(0)()
+            yield
+
+    def run(self, agents, issuer, max_steps=2000000):
+        def issuer_wrapper():
+            yield from issuer
+            self.issuer_done = True
+        self.live = list(agents) + [issuer_wrapper(), self._pipe()]
+        steps = 0
+        while self.live:
+            a = self.rng.choice(self.live)
+            try:
+                next(a)
+            except StopIteration:
+                self.live.remove(a)
+            steps += 1
+            assert steps < max_steps, "deadlock: no agent can make progress"
+
+
+# ------------------------------------------------------------------------------------------
+# Forward kernel (dense, one CTA = two 128-row query tiles).  nsteps[t]: key steps of query tile
+# t (128-key tiles, or 64-key half steps when half=True); S: K/V ring stages.
+
+def forward(nsteps, S, half, seed, bug=None):
+    """`bug` = "early_k_release" plants a known protocol error: each K stage is released before
+    the S MMAs of its step (or half step) have been issued."""
+    n0, n1 = nsteps
+    assert n1 == 0 or n0 > 0
+    nmax = max(n0, n1)
+    npos = (nmax + 1) // 2 if half else nmax  # 128-key K/V stages the producer loads
+    sim = Sim(seed)
+    q_full = Bar(1, "q_full")
+    k_full = [Bar(1, f"k_full{s}") for s in range(S)]
+    k_empty = [Bar(1, f"k_empty{s}") for s in range(S)]
+    v_full = [Bar(1, f"v_full{s}") for s in range(S)]
+    v_empty = [Bar(1, f"v_empty{s}") for s in range(S)]
+    s_full = [Bar(1, f"s_full{t}") for t in range(2)]
+    p_full = [Bar(4, f"p_full{t}") for t in range(2)]
+    o_full = [Bar(1, f"o_full{t}") for t in range(2)]
+    Kst = [Buf(f"K{s}") for s in range(S)]
+    Vst = [Buf(f"V{s}") for s in range(S)]
+    Qt = [Buf(f"Q{t}") for t in range(2)]
+    # tensor memory: S/P of tile t per 32-lane quadrant; O of tile t as the count of P V applied
+    Sreg = [[Buf(f"S{t}q{q}") for q in range(4)] for t in range(2)]
+    O = [0, 0]
+    done = {"S": [[], []], "PV": [[], []]}
+
+    def readers_of(j):  # S (K) or P V (V) MMAs that read stage position j
+        if half:
+            return sum(1 for t in range(2) for h in range(2) if 2 * j + h < nsteps[t])
+        return sum(1 for t in range(2) if j < nsteps[t])
+
+    def load(buf, val, readers, bar):
+        def fn():
+            buf.write(val, readers=readers)
+            bar.arrive()
+        sim.copy(fn)
+
+    def producer():
+        if npos == 0:
+            return
+        ntiles = 2 if n1 > 0 else 1
+
+        def q_copy():
+            for t in range(ntiles):
+                Qt[t].write("Q")
+            q_full.arrive()
+        sim.copy(q_copy)
+        for j in range(npos):
+            s, ph = j % S, (j // S) & 1
+            yield from wait(k_empty[s], ph ^ 1, j // S)
+            load(Kst[s], j, readers_of(j), k_full[s])
+            yield from wait(v_empty[s], ph ^ 1, j // S)
+            load(Vst[s], j, readers_of(j), v_full[s])
+
+    def op_S(t, step, s, j):
+        def fn():
+            Qt[t].read("Q")
+            Kst[s].read(j, consume=True)
+            for q in range(4):
+                Sreg[t][q].write(("S", step), readers=1)
+            done["S"][t].append(step)
+        sim.issue(fn)
+
+    def op_PV(t, step, sp, jp):
+        def fn():
+            for q in range(4):
+                Sreg[t][q].read(("P", step), consume=True)
+            Vst[sp].read(jp, consume=True)
+            assert O[t] == step
+            O[t] += 1
+            done["PV"][t].append(step)
+        sim.issue(fn)
+
+    def commit(bar):
+        sim.issue(bar.arrive)
+
+    def mma():
+        if npos == 0:
+            return
+        yield from wait(q_full, 0, 1)
+        cnt = [0, 0]
+        if half:
+            for hs in range(nmax + 1):
+                j, hf = hs >> 1, hs & 1
+                s = j % S
+                jp, hp = (hs - 1) >> 1, (hs - 1) & 1
+                sp = jp % S if hs >= 1 else 0
+                if hs < nmax and hf == 0:
+                    yield from wait(k_full[s], (j // S) & 1, j // S + 1)
+                if hs >= 1 and hp == 0:
+                    yield from wait(v_full[sp], (jp // S) & 1, jp // S + 1)
+                k_release = hs < nmax and (hf == 1 or hs == nmax - 1)
+                if bug == "early_k_release" and k_release:
+                    commit(k_empty[s])
+                for t in range(2):
+                    if hs >= 1 and hs - 1 < nsteps[t]:
+                        yield from wait(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        op_PV(t, hs - 1, sp, jp)
+                        if cnt[t] == nsteps[t]:
+                            commit(o_full[t])
+                    if hs < nsteps[t]:
+                        op_S(t, hs, s, j)
+                        commit(s_full[t])
+                        cnt[t] += 1
+                if k_release and bug != "early_k_release":
+                    commit(k_empty[s])
+                if hs >= 1 and (hp == 1 or hs - 1 == nmax - 1):
+                    commit(v_empty[sp])
+        else:
+            use_prev = 0
+            for j in range(npos + 1):
+                s, sp = j % S, (j + S - 1) % S
+                use = ((1 if j < n0 else 0) | (2 if j < n1 else 0)) if j < npos else 0
+                if j < npos:
+                    yield from wait(k_full[s], (j // S) & 1, j // S + 1)
+                if j >= 1:
+                    yield from wait(v_full[sp], ((j - 1) // S) & 1, (j - 1) // S + 1)
+                if bug == "early_k_release" and j < npos:
+                    commit(k_empty[s])
+                for t in range(2):
+                    if (use_prev >> t) & 1:
+                        yield from wait(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        op_PV(t, j - 1, sp, j - 1)
+                        if cnt[t] == nsteps[t]:
+                            commit(o_full[t])
+                    if (use >> t) & 1:
+                        op_S(t, j, s, j)
+                        commit(s_full[t])
+                        cnt[t] += 1
+                if j < npos and bug != "early_k_release":
+                    commit(k_empty[s])
+                if j >= 1:
+                    commit(v_empty[sp])
+                use_prev = use
+
+    def softmax(t, q):
+        n = nsteps[t]
+        for j in range(n):
+            yield from wait(s_full[t], j & 1, j + 1)
+            Sreg[t][q].read(("S", j), consume=True)
+            # rescaling O~ needs every earlier P V of the tile to have completed
+            assert O[t] == j, f"O{t}: {O[t]} P V applied at softmax step {j}"
+            Sreg[t][q].write(("P", j), readers=1)
+            p_full[t].arrive()
+        if n > 0:
+            yield from wait(o_full[t], 0, 1)
+            assert O[t] == n
+
+    sim.run([producer()] + [softmax(t, q) for t in range(2) for q in range(4)], mma())
+    for t in range(2):
+        assert done["S"][t] == list(range(nsteps[t])), done
+        assert done["PV"][t] == list(range(nsteps[t])), done
+
+
+# ------------------------------------------------------------------------------------------
+# dK/dV kernel (bwd_dkdv_kernel with the dQ MMA and drain): one key tile, nit query iterations;
+# two Q (with its LSE, D rows) and two dO stages; `groups` elementwise warpgroups, each owning
+# its share of the query columns of S^T / dP^T and of the dQ columns, per 32-lane quadrant (the
+# d = 128 column layout: a group's dQ columns are its own dS columns).
+
+def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
+    """`bug` plants a protocol error (for the tests that show the checker catches it):
+    "dv_before_do": dV(i+1) issued before waiting for dO(i+1)'s copy (a race once present in the
+    kernel); "early_q_release": Q_i's stage released before dK(i), its last reader.
+    ("early_do_release", dO(i+1)'s stage released right after dV(i+1) and before dP(i+1), is
+    harmless under this producer order: the producer refills that stage only after Q_(i+3)'s
+    stage, which dK(i+1) releases after dP(i+1) has run; the tests show that too.)"""
+    sim = Sim(seed)
+    W = 4 * groups  # elementwise warps
+    kv_full = Bar(1, "kv_full")
+    q_full = [Bar(1, f"q_full{s}") for s in range(2)]
+    q_empty = [Bar(1, f"q_empty{s}") for s in range(2)]
+    do_full = [Bar(1, f"do_full{s}") for s in range(2)]
+    do_empty = [Bar(1, f"do_empty{s}") for s in range(2)]
+    s_full, dp_full = Bar(1, "s_full"), Bar(1, "dp_full")
+    p_full, ds_full, dq_empty = Bar(W, "p_full"), Bar(W, "ds_full"), Bar(W, "dq_empty")
+    dq_full, dkdv_full = Bar(1, "dq_full"), Bar(1, "dkdv_full")
+    KV = Buf("KV")
+    Qst = [Buf(f"Q{s}") for s in range(2)]
+    dOst = [Buf(f"dO{s}") for s in range(2)]
+    cells = [(g, q) for g in range(groups) for q in range(4)]
+    Sreg = {c: Buf(f"S{c}") for c in cells}    # S^T, then P^T
+    DPreg = {c: Buf(f"DP{c}") for c in cells}  # dP^T, then dS^T, then dQ
+    DS = {c: Buf(f"dS{c}") for c in cells}     # dS in shared memory (A operand of dQ = dS K)
+    acc = {"dV": 0, "dK": 0}
+    drained = [[] for _ in cells]
+
+    def producer():
+        if nit == 0:
+            return
+
+        def kv_copy():
+            KV.write("KV")
+            kv_full.arrive()
+        sim.copy(kv_copy)
+        for it in range(nit):
+            s, ph = it & 1, (it >> 1) & 1
+            yield from wait(q_empty[s], ph ^ 1, it >> 1)
+
+            # Q_i is read by S(i) and dK(i), its LSE and D rows by every elementwise warp (for
+            # P and for dS); dO_i by dP(i) and dV(i)
+            def q_copy(s=s, it=it):
+                Qst[s].write(it, readers=2 + 2 * W)
+                q_full[s].arrive()
+            sim.copy(q_copy)
+            yield from wait(do_empty[s], ph ^ 1, it >> 1)
+
+            def do_copy(s=s, it=it):
+                dOst[s].write(it, readers=2)
+                do_full[s].arrive()
+            sim.copy(do_copy)
+
+    def mma():
+        if nit == 0:
+            return
+
+        def issue_S(it):
+            def fn():
+                KV.read("KV")
+                Qst[it & 1].read(it, consume=True)
+                for c in cells:
+                    Sreg[c].write(("S", it), readers=1)
+            sim.issue(fn)
+            sim.issue(s_full.arrive)
+
+        def issue_dP(it):
+            def fn():
+                KV.read("KV")
+                dOst[it & 1].read(it, consume=True)
+                for c in cells:
+                    DPreg[c].write(("dP", it), readers=1)
+            sim.issue(fn)
+            sim.issue(dp_full.arrive)
+
+        def issue_dV(it):
+            def fn():
+                for c in cells:
+                    Sreg[c].read(("P", it), consume=True)
+                dOst[it & 1].read(it, consume=True)
+                assert acc["dV"] == it
+                acc["dV"] += 1
+            sim.issue(fn)
+
+        def release_do(it):
+            sim.issue(do_empty[it & 1].arrive)
+
+        def issue_dK_dQ(it):
+            def dk():
+                for c in cells:
+                    DPreg[c].read(("dS", it), consume=True)
+                Qst[it & 1].read(it, consume=True)
+                assert acc["dK"] == it
+                acc["dK"] += 1
+            if bug == "early_q_release":
+                sim.issue(q_empty[it & 1].arrive)
+            sim.issue(dk)
+            if bug != "early_q_release":
+                sim.issue(q_empty[it & 1].arrive)
+            if with_dq:
+                def dq():
+                    KV.read("KV")
+                    for c in cells:
+                        DS[c].read(("dS", it), consume=True)
+                    for c in cells:
+                        DPreg[c].write(("dQ", it), readers=1)
+                sim.issue(dq)
+                sim.issue(dq_full.arrive)
+
+        def wait_q(it):
+            yield from wait(q_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)
+
+        def wait_do(it):
+            yield from wait(do_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)
+
+        yield from wait(kv_full, 0, 1)
+        yield from wait_q(0)
+        issue_S(0)
+        yield from wait_do(0)
+        issue_dP(0)
+        yield from wait(p_full, 0, 1)
+        issue_dV(0)
+        release_do(0)
+        if nit > 1:
+            yield from wait_q(1)
+            issue_S(1)
+        for it in range(nit):
+            yield from wait(ds_full, it & 1, it + 1)
+            issue_dK_dQ(it)
+            if it + 1 < nit:
+                yield from wait(p_full, (it + 1) & 1, it + 2)
+                if bug != "dv_before_do":
+                    yield from wait_do(it + 1)
+                issue_dV(it + 1)
+                if bug == "dv_before_do":
+                    yield from wait_do(it + 1)
+                if bug == "early_do_release":
+                    release_do(it + 1)
+                if with_dq:
+                    yield from wait(dq_empty, it & 1, it + 1)
+                issue_dP(it + 1)
+                if bug != "early_do_release":
+                    release_do(it + 1)
+                if it + 2 < nit:
+                    yield from wait_q(it + 2)
+                    issue_S(it + 2)
+        sim.issue(dkdv_full.arrive)
+
+    def elementwise(c, k):
+        def drain(it):
+            yield from wait(dq_full, it & 1, it + 1)
+            DPreg[c].read(("dQ", it), consume=True)
+            drained[k].append(it)
+            dq_empty.arrive()
+
+        for it in range(nit):
+            s, ph = it & 1, (it >> 1) & 1
+            yield from wait(q_full[s], ph, (it >> 1) + 1)
+            Qst[s].read(it, consume=True)  # the LSE and D rows of this query tile
+            yield from wait(s_full, it & 1, it + 1)
+            Sreg[c].read(("S", it), consume=True)
+            Sreg[c].write(("P", it), readers=1)
+            p_full.arrive()
+            if with_dq and it > 0:
+                yield from drain(it - 1)
+            yield from wait(dp_full, it & 1, it + 1)
+            DPreg[c].read(("dP", it), consume=True)
+            Qst[s].read(it, consume=True)
+            DPreg[c].write(("dS", it), readers=1)
+            if with_dq:
+                DS[c].write(("dS", it), readers=1)
+            ds_full.arrive()
+        if with_dq and nit > 0:
+            yield from drain(nit - 1)
+        if nit > 0:
+            yield from wait(dkdv_full, 0, 1)
+            assert acc["dV"] == nit and acc["dK"] == nit
+
+    sim.run([producer()] + [elementwise(c, k) for k, c in enumerate(cells)], mma())
+    assert acc == {"dV": nit, "dK": nit}
+    if with_dq:
+        assert all(d == list(range(nit)) for d in drained)

@@ -1,0 +1,56 @@
+"""CPU model check of the kernels' mbarrier pipelines (tests/protocol_model.py): the forward
+(128-key steps and the d = 64 half steps) and the dK/dV kernel run their roles' waits, arrivals
+and buffer reads and writes under many random interleavings, for every per-tile step count up to
+a few stages past the ring's length; no deadlock, no wait on a wrong phase, no read of a stage
+before its copy or after its release.  Planted protocol errors (among them the dO race once found in
+the dK/dV kernel) must fail."""
+
+import pytest
+
+from protocol_model import dkdv, forward
+
+
+def _tile_steps(nmax):
+    # tile 1 never has steps without tile 0 (its rows come after tile 0's); under a causal mask
+    # it has more, without one the same
+    return [(a, b) for a in range(nmax + 1) for b in range(nmax + 1) if not (a == 0 and b > 0)]
+
+
+@pytest.mark.parametrize("half,S", [(False, 2), (False, 4), (True, 2)],
+                         ids=["128-key-2-stages", "128-key-4-stages", "half-step-2-stages"])
+def test_forward_protocol(half, S):
+    for n0, n1 in _tile_steps(9):
+        for seed in range(8):
+            forward((n0, n1), S, half, seed)
+
+
+@pytest.mark.parametrize("groups", [2, 4])
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_dkdv_protocol(groups, with_dq):
+    for nit in range(0, 9):
+        for seed in range(12):
+            dkdv(nit, seed, groups=groups, with_dq=with_dq)
+
+
+def _fails(fn):
+    for seed in range(200):
+        try:
+            fn(seed)
+        except AssertionError:
+            return True
+    return False
+
+
+@pytest.mark.parametrize("bug", ["dv_before_do", "early_q_release"])
+def test_checker_catches_dkdv_protocol_errors(bug):
+    assert _fails(lambda seed: dkdv(6, seed, bug=bug))
+
+
+def test_early_do_release_is_harmless_under_this_producer_order():
+    for seed in range(100):
+        dkdv(6, seed, bug="early_do_release")
+
+
+@pytest.mark.parametrize("half", [False, True])
+def test_checker_catches_an_early_stage_release(half):
+    assert _fails(lambda seed: forward((5, 7), 2, half, seed, bug="early_k_release"))
