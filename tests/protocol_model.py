@@ -23,7 +23,7 @@ A missing wait lets some interleaving read a stage before its copy lands; a rele
 last reader lets the producer overwrite a stage that is still needed; both fail here.  The models
 follow the kernels' code (fa_fwd.cu: fwd_kernel's producer, MMA issuer and softmax warpgroups,
 dense and half-step; fa_bwd.cu: bwd_dkdv_kernel's producer, MMA issuer and elementwise
-warpgroups) and must change with it.
+warpgroups; fa_bwd_dq.cu: bwd_dq_kernel's) and must change with it.
 """
 
 from __future__ import annotations
@@ -468,3 +468,126 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
     assert acc == {"dV": nit, "dK": nit}
     if with_dq:
         assert all(d == list(range(nit)) for d in drained)
+
+
+# ------------------------------------------------------------------------------------------
+# Deterministic dQ kernel (bwd_dq_kernel): one query tile, nb key tiles; Q_i and dO_i loaded
+# once, K_j and V_j through two stages each; S in one tensor-memory region, dP (then dS) in two
+# alternating ones; two warpgroups of 64 keys each.
+
+def dq_kernel(nb, seed, bug=None):
+    """`bug` = "s_before_read" plants a protocol error: S(j+1) issued without waiting for the
+    warps to have read S(j)."""
+    sim = Sim(seed)
+    W = 8
+    qdo_full = Bar(1, "qdo_full")
+    k_full = [Bar(1, f"k_full{s}") for s in range(2)]
+    k_empty = [Bar(1, f"k_empty{s}") for s in range(2)]
+    v_full = [Bar(1, f"v_full{s}") for s in range(2)]
+    v_empty = [Bar(1, f"v_empty{s}") for s in range(2)]
+    s_full, s_read = Bar(1, "s_full"), Bar(W, "s_read")
+    dp_full = [Bar(1, f"dp_full{b}") for b in range(2)]
+    ds_full = [Bar(W, f"ds_full{b}") for b in range(2)]
+    dq_full = Bar(1, "dq_full")
+    QdO = Buf("QdO")
+    Kst = [Buf(f"K{s}") for s in range(2)]
+    Vst = [Buf(f"V{s}") for s in range(2)]
+    cells = [(g, q) for g in range(2) for q in range(4)]
+    Sreg = {c: Buf(f"S{c}") for c in cells}
+    DPreg = [{c: Buf(f"DP{b}{c}") for c in cells} for b in range(2)]
+    acc = {"dQ": 0}
+
+    def producer():
+        if nb == 0:
+            return
+
+        def qdo():
+            QdO.write("QdO")
+            qdo_full.arrive()
+        sim.copy(qdo)
+        for jj in range(nb):
+            s, ph = jj & 1, (jj >> 1) & 1
+            yield from wait(k_empty[s], ph ^ 1, jj >> 1)
+
+            def k_copy(s=s, jj=jj):
+                Kst[s].write(jj, readers=2)  # S(j) and dQ(j)
+                k_full[s].arrive()
+            sim.copy(k_copy)
+            yield from wait(v_empty[s], ph ^ 1, jj >> 1)
+
+            def v_copy(s=s, jj=jj):
+                Vst[s].write(jj, readers=1)  # dP(j)
+                v_full[s].arrive()
+            sim.copy(v_copy)
+
+    def mma():
+        if nb == 0:
+            return
+
+        def issue_S(jj):
+            def fn():
+                QdO.read("QdO")
+                Kst[jj & 1].read(jj, consume=True)
+                for c in cells:
+                    Sreg[c].write(("S", jj), readers=1)
+            sim.issue(fn)
+            sim.issue(s_full.arrive)
+
+        def issue_dP(jj):
+            def fn():
+                QdO.read("QdO")
+                Vst[jj & 1].read(jj, consume=True)
+                for c in cells:
+                    DPreg[jj & 1][c].write(("dP", jj), readers=1)
+            sim.issue(fn)
+            sim.issue(dp_full[jj & 1].arrive)
+            sim.issue(v_empty[jj & 1].arrive)
+
+        def issue_dQ(jj):
+            def fn():
+                for c in cells:
+                    DPreg[jj & 1][c].read(("dS", jj), consume=True)
+                Kst[jj & 1].read(jj, consume=True)
+                assert acc["dQ"] == jj
+                acc["dQ"] += 1
+            sim.issue(fn)
+            sim.issue(k_empty[jj & 1].arrive)
+
+        def wait_k(jj):
+            yield from wait(k_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+
+        def wait_v(jj):
+            yield from wait(v_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+
+        yield from wait(qdo_full, 0, 1)
+        yield from wait_k(0)
+        issue_S(0)
+        yield from wait_v(0)
+        issue_dP(0)
+        for jj in range(nb):
+            if jj + 1 < nb:
+                if bug != "s_before_read":
+                    yield from wait(s_read, jj & 1, jj + 1)
+                yield from wait_k(jj + 1)
+                issue_S(jj + 1)
+                yield from wait_v(jj + 1)
+                issue_dP(jj + 1)
+            yield from wait(ds_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            issue_dQ(jj)
+        sim.issue(dq_full.arrive)
+
+    def elementwise(c):
+        for jj in range(nb):
+            yield from wait(s_full, jj & 1, jj + 1)
+            Sreg[c].read(("S", jj), consume=True)
+            s_read.arrive()
+            yield from wait(dp_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            DPreg[jj & 1][c].read(("dP", jj), consume=True)
+            DPreg[jj & 1][c].write(("dS", jj), readers=1)
+            ds_full[jj & 1].arrive()
+        if nb > 0:
+            yield from wait(dq_full, 0, 1)
+            assert acc["dQ"] == nb
+
+    sim.run([producer()] + [elementwise(c) for c in cells], mma())
+    assert acc["dQ"] == nb

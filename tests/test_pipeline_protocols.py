@@ -1,5 +1,5 @@
 """CPU model check of the kernels' mbarrier pipelines (tests/protocol_model.py): the forward
-(128-key steps and the d = 64 half steps) and the dK/dV kernel run their roles' waits, arrivals
+(128-key steps and the d = 64 half steps), the dK/dV kernel and the deterministic dQ kernel run their roles' waits, arrivals
 and buffer reads and writes under many random interleavings, for every per-tile step count up to
 a few stages past the ring's length; no deadlock, no wait on a wrong phase, no read of a stage
 before its copy or after its release.  Planted protocol errors (among them the dO race once found in
@@ -7,7 +7,7 @@ the dK/dV kernel) must fail."""
 
 import pytest
 
-from protocol_model import dkdv, forward
+from protocol_model import dkdv, dq_kernel, forward
 
 
 def _tile_steps(nmax):
@@ -32,6 +32,12 @@ def test_dkdv_protocol(groups, with_dq):
             dkdv(nit, seed, groups=groups, with_dq=with_dq)
 
 
+def test_deterministic_dq_protocol():
+    for nb in range(0, 10):
+        for seed in range(12):
+            dq_kernel(nb, seed)
+
+
 def _fails(fn):
     for seed in range(200):
         try:
@@ -54,3 +60,7 @@ def test_early_do_release_is_harmless_under_this_producer_order():
 @pytest.mark.parametrize("half", [False, True])
 def test_checker_catches_an_early_stage_release(half):
     assert _fails(lambda seed: forward((5, 7), 2, half, seed, bug="early_k_release"))
+
+
+def test_checker_catches_an_overwrite_of_unread_scores():
+    assert _fails(lambda seed: dq_kernel(6, seed, bug="s_before_read"))
