@@ -129,13 +129,20 @@ class Sim:
 # Forward kernel (dense, one CTA = two 128-row query tiles).  nsteps[t]: key steps of query tile
 # t (128-key tiles, or 64-key half steps when half=True); S: K/V ring stages.
 
-def forward(nsteps, S, half, seed, bug=None):
+def forward(nsteps, S, half, seed, bug=None, uses=None):
     """`bug` = "early_k_release" plants a known protocol error: each K stage is released before
-    the S MMAs of its step (or half step) have been issued."""
+    the S MMAs of its step (or half step) have been issued.  `uses` (block-sparse, 128-key steps):
+    per position of the K/V stream a nonzero bit mask of the query tiles that keep that key tile;
+    nsteps is then derived from it."""
+    if uses is not None:
+        assert not half and all(u in (1, 2, 3) for u in uses)
+        nsteps = (sum(u & 1 for u in uses), sum((u >> 1) & 1 for u in uses))
     n0, n1 = nsteps
-    assert n1 == 0 or n0 > 0
+    assert uses is not None or n1 == 0 or n0 > 0  # dense: tile 1's rows come after tile 0's
     nmax = max(n0, n1)
     npos = (nmax + 1) // 2 if half else nmax  # 128-key K/V stages the producer loads
+    if uses is not None:
+        npos = len(uses)
     sim = Sim(seed)
     q_full = Bar(1, "q_full")
     k_full = [Bar(1, f"k_full{s}") for s in range(S)]
@@ -154,6 +161,8 @@ def forward(nsteps, S, half, seed, bug=None):
     done = {"S": [[], []], "PV": [[], []]}
 
     def readers_of(j):  # S (K) or P V (V) MMAs that read stage position j
+        if uses is not None:
+            return bin(uses[j]).count("1")
         if half:
             return sum(1 for t in range(2) for h in range(2) if 2 * j + h < nsteps[t])
         return sum(1 for t in range(2) if j < nsteps[t])
@@ -181,7 +190,7 @@ def forward(nsteps, S, half, seed, bug=None):
             yield from wait(v_empty[s], ph ^ 1, j // S)
             load(Vst[s], j, readers_of(j), v_full[s])
 
-    def op_S(t, step, s, j):
+    def op_S(t, step, s, j):  # `step`: the tile's own count of S (its softmax step)
         def fn():
             Qt[t].read("Q")
             Kst[s].read(j, consume=True)
@@ -239,21 +248,32 @@ def forward(nsteps, S, half, seed, bug=None):
             use_prev = 0
             for j in range(npos + 1):
                 s, sp = j % S, (j + S - 1) % S
-                use = ((1 if j < n0 else 0) | (2 if j < n1 else 0)) if j < npos else 0
+                if uses is not None:
+                    use = uses[j] if j < npos else 0
+                else:
+                    use = ((1 if j < n0 else 0) | (2 if j < n1 else 0)) if j < npos else 0
                 if j < npos:
                     yield from wait(k_full[s], (j // S) & 1, j // S + 1)
                 if j >= 1:
                     yield from wait(v_full[sp], ((j - 1) // S) & 1, (j - 1) // S + 1)
                 if bug == "early_k_release" and j < npos:
                     commit(k_empty[s])
+                if uses is not None:
+                    # block-sparse: a tile that starts a use here, with no P V pending, gets its
+                    # S first (its softmax step is its own count of S)
+                    for t in range(2):
+                        if ((use >> t) & 1) and not ((use_prev >> t) & 1):
+                            op_S(t, cnt[t], s, j)
+                            commit(s_full[t])
+                            cnt[t] += 1
                 for t in range(2):
                     if (use_prev >> t) & 1:
                         yield from wait(p_full[t], (cnt[t] - 1) & 1, cnt[t])
-                        op_PV(t, j - 1, sp, j - 1)
+                        op_PV(t, cnt[t] - 1, sp, j - 1)
                         if cnt[t] == nsteps[t]:
                             commit(o_full[t])
-                    if (use >> t) & 1:
-                        op_S(t, j, s, j)
+                    if ((use >> t) & 1) and (uses is None or ((use_prev >> t) & 1)):
+                        op_S(t, cnt[t], s, j)
                         commit(s_full[t])
                         cnt[t] += 1
                 if j < npos and bug != "early_k_release":

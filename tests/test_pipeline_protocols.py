@@ -1,5 +1,5 @@
 """CPU model check of the kernels' mbarrier pipelines (tests/protocol_model.py): the forward
-(128-key steps and the d = 64 half steps), the dK/dV kernel and the deterministic dQ kernel run their roles' waits, arrivals
+(128-key steps, block-sparse streams with gaps, the d = 64 half steps), the dK/dV kernel and the deterministic dQ kernel run their roles' waits, arrivals
 and buffer reads and writes under many random interleavings, for every per-tile step count up to
 a few stages past the ring's length; no deadlock, no wait on a wrong phase, no read of a stage
 before its copy or after its release.  Planted protocol errors (among them the dO race once found in
@@ -22,6 +22,19 @@ def test_forward_protocol(half, S):
     for n0, n1 in _tile_steps(9):
         for seed in range(8):
             forward((n0, n1), S, half, seed)
+
+
+@pytest.mark.parametrize("S", [2, 4])
+def test_block_sparse_forward_protocol(S):
+    """Block-sparse K/V streams: each position is kept by tile 0, tile 1 or both, with gaps."""
+    import random
+
+    rng = random.Random(5)
+    for length in range(1, 9):
+        for _ in range(20):
+            uses = [rng.choice((1, 2, 3)) for _ in range(length)]
+            for seed in range(4):
+                forward(None, S, False, seed, uses=uses)
 
 
 @pytest.mark.parametrize("groups", [2, 4])
