@@ -77,13 +77,37 @@ class Sim:
     order at times of its own, and the copy engine, whose copies each land at a time of their
     own."""
 
-    def __init__(self, seed):
+    def __init__(self, seed, abort_at=None):
         import random
 
         self.rng = random.Random(seed)
         self.live = []
         self.queue = []          # tensor pipe: operations in issue order
         self.issuer_done = False
+        self.copies = 0          # copies issued and not yet landed
+        self.abort = False       # the CTA's abort flag
+        self.abort_at = abort_at  # the spinning wait that runs past its time limit (None: none)
+        self.spins = 0
+
+    def wait_ok(self, bar, parity, completed):
+        """Generator for a bounded wait (mbar_wait): True once the phase has completed; False
+        when another role has aborted, or when this wait is the one chosen to time out (it then
+        sets the abort flag)."""
+        while not bar.try_wait(parity):
+            if self.abort:
+                return False
+            self.spins += 1
+            if self.abort_at is not None and self.spins == self.abort_at:
+                self.abort = True
+                return False
+            yield
+        assert bar.c == completed, f"{bar.name}: passed with {bar.c} completed phases, meant {completed}"
+        return True
+
+    def drain(self, bar, parity):
+        """Generator for drain_wait: waits for the phase regardless of the abort flag."""
+        while not bar.try_wait(parity):
+            yield
 
     def spawn(self, gen):
         self.live.append(gen)
@@ -92,11 +116,13 @@ class Sim:
         """An asynchronous copy: `fn` (write the stage, arrive on its barrier) runs after a random
         delay, long enough for the consumers to race ahead of it."""
         delay = self.rng.randint(0, 40)
+        self.copies += 1
 
         def agent():
             for _ in range(delay + 1):
                 yield
             fn()
+            self.copies -= 1
         self.spawn(agent())
 
     def issue(self, fn):
@@ -110,10 +136,23 @@ class Sim:
             yield
 
     def run(self, agents, issuer, max_steps=2000000):
+        """Run the roles (and the engines) to completion, and record what is still in flight when
+        the last role finishes — the CTA exits: `exit_copies` copies, `exit_ops` queued MMA
+        operations.  Both must be 0: a copy landing in the shared memory of a CTA that has exited
+        would write into the next CTA's.  The callers assert it."""
+        roles = {"left": len(agents) + 1}
+        self.exit_copies = self.exit_ops = None
+
+        def role(gen):
+            yield from gen
+            roles["left"] -= 1
+            if roles["left"] == 0:
+                self.exit_copies, self.exit_ops = self.copies, len(self.queue)
+
         def issuer_wrapper():
             yield from issuer
             self.issuer_done = True
-        self.live = list(agents) + [issuer_wrapper(), self._pipe()]
+        self.live = [role(a) for a in agents] + [role(issuer_wrapper()), self._pipe()]
         steps = 0
         while self.live:
             a = self.rng.choice(self.live)
@@ -129,11 +168,15 @@ class Sim:
 # Forward kernel (dense, one CTA = two 128-row query tiles).  nsteps[t]: key steps of query tile
 # t (128-key tiles, or 64-key half steps when half=True); S: K/V ring stages.
 
-def forward(nsteps, S, half, seed, bug=None, uses=None):
+def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, drain_always=False):
     """`bug` = "early_k_release" plants a known protocol error: each K stage is released before
     the S MMAs of its step (or half step) have been issued.  `uses` (block-sparse, 128-key steps):
     per position of the K/V stream a nonzero bit mask of the query tiles that keep that key tile;
-    nsteps is then derived from it."""
+    nsteps is then derived from it.  `abort_at`: the abort_at-th spin of any bounded wait runs
+    past its time limit (the kernel's timeout path); every role must then leave, with no MMA
+    queued.  `drain_always`: the producer waits for its last copies whether or not the CTA has
+    aborted (the kernel waits only when the abort flag is already set as its producer leaves its
+    loop; see test_pipeline_protocols.py).  Returns the Sim (its spin count, exit state)."""
     if uses is not None:
         assert not half and all(u in (1, 2, 3) for u in uses)
         nsteps = (sum(u & 1 for u in uses), sum((u >> 1) & 1 for u in uses))
@@ -143,7 +186,8 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
     npos = (nmax + 1) // 2 if half else nmax  # 128-key K/V stages the producer loads
     if uses is not None:
         npos = len(uses)
-    sim = Sim(seed)
+    sim = Sim(seed, abort_at)
+    wait_ok = sim.wait_ok
     q_full = Bar(1, "q_full")
     k_full = [Bar(1, f"k_full{s}") for s in range(S)]
     k_empty = [Bar(1, f"k_empty{s}") for s in range(S)]
@@ -152,6 +196,7 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
     s_full = [Bar(1, f"s_full{t}") for t in range(2)]
     p_full = [Bar(4, f"p_full{t}") for t in range(2)]
     o_full = [Bar(1, f"o_full{t}") for t in range(2)]
+    mma_done = Bar(1, "mma_done")
     Kst = [Buf(f"K{s}") for s in range(S)]
     Vst = [Buf(f"V{s}") for s in range(S)]
     Qt = [Buf(f"Q{t}") for t in range(2)]
@@ -183,12 +228,24 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
                 Qt[t].write("Q")
             q_full.arrive()
         sim.copy(q_copy)
+        jk = jv = 0  # K and V copies issued
         for j in range(npos):
             s, ph = j % S, (j // S) & 1
-            yield from wait(k_empty[s], ph ^ 1, j // S)
+            if not (yield from wait_ok(k_empty[s], ph ^ 1, j // S)):
+                break
             load(Kst[s], j, readers_of(j), k_full[s])
-            yield from wait(v_empty[s], ph ^ 1, j // S)
+            jk = j + 1
+            if not (yield from wait_ok(v_empty[s], ph ^ 1, j // S)):
+                break
             load(Vst[s], j, readers_of(j), v_full[s])
+            jv = j + 1
+        if sim.abort or drain_always:
+            # no copy into this CTA's shared memory may still be in flight when it exits
+            yield from sim.drain(q_full, 0)
+            for jj in range(max(0, jk - S), jk):
+                yield from sim.drain(k_full[jj % S], (jj // S) & 1)
+            for jj in range(max(0, jv - S), jv):
+                yield from sim.drain(v_full[jj % S], (jj // S) & 1)
 
     def op_S(t, step, s, j):  # `step`: the tile's own count of S (its softmax step)
         def fn():
@@ -215,24 +272,31 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
     def mma():
         if npos == 0:
             return
-        yield from wait(q_full, 0, 1)
+        ok = yield from wait_ok(q_full, 0, 1)
         cnt = [0, 0]
         if half:
-            for hs in range(nmax + 1):
+            hs = 0
+            while ok and hs <= nmax:
                 j, hf = hs >> 1, hs & 1
                 s = j % S
                 jp, hp = (hs - 1) >> 1, (hs - 1) & 1
                 sp = jp % S if hs >= 1 else 0
                 if hs < nmax and hf == 0:
-                    yield from wait(k_full[s], (j // S) & 1, j // S + 1)
+                    ok = yield from wait_ok(k_full[s], (j // S) & 1, j // S + 1)
+                    if not ok:
+                        break
                 if hs >= 1 and hp == 0:
-                    yield from wait(v_full[sp], (jp // S) & 1, jp // S + 1)
+                    ok = yield from wait_ok(v_full[sp], (jp // S) & 1, jp // S + 1)
+                    if not ok:
+                        break
                 k_release = hs < nmax and (hf == 1 or hs == nmax - 1)
                 if bug == "early_k_release" and k_release:
                     commit(k_empty[s])
                 for t in range(2):
                     if hs >= 1 and hs - 1 < nsteps[t]:
-                        yield from wait(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        ok = yield from wait_ok(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        if not ok:
+                            break
                         op_PV(t, hs - 1, sp, jp)
                         if cnt[t] == nsteps[t]:
                             commit(o_full[t])
@@ -240,22 +304,30 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
                         op_S(t, hs, s, j)
                         commit(s_full[t])
                         cnt[t] += 1
+                if not ok:
+                    break
                 if k_release and bug != "early_k_release":
                     commit(k_empty[s])
                 if hs >= 1 and (hp == 1 or hs - 1 == nmax - 1):
                     commit(v_empty[sp])
+                hs += 1
         else:
             use_prev = 0
-            for j in range(npos + 1):
+            j = 0
+            while ok and j <= npos:
                 s, sp = j % S, (j + S - 1) % S
                 if uses is not None:
                     use = uses[j] if j < npos else 0
                 else:
                     use = ((1 if j < n0 else 0) | (2 if j < n1 else 0)) if j < npos else 0
                 if j < npos:
-                    yield from wait(k_full[s], (j // S) & 1, j // S + 1)
+                    ok = yield from wait_ok(k_full[s], (j // S) & 1, j // S + 1)
+                    if not ok:
+                        break
                 if j >= 1:
-                    yield from wait(v_full[sp], ((j - 1) // S) & 1, (j - 1) // S + 1)
+                    ok = yield from wait_ok(v_full[sp], ((j - 1) // S) & 1, (j - 1) // S + 1)
+                    if not ok:
+                        break
                 if bug == "early_k_release" and j < npos:
                     commit(k_empty[s])
                 if uses is not None:
@@ -268,7 +340,9 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
                             cnt[t] += 1
                 for t in range(2):
                     if (use_prev >> t) & 1:
-                        yield from wait(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        ok = yield from wait_ok(p_full[t], (cnt[t] - 1) & 1, cnt[t])
+                        if not ok:
+                            break
                         op_PV(t, cnt[t] - 1, sp, j - 1)
                         if cnt[t] == nsteps[t]:
                             commit(o_full[t])
@@ -276,29 +350,43 @@ def forward(nsteps, S, half, seed, bug=None, uses=None):
                         op_S(t, cnt[t], s, j)
                         commit(s_full[t])
                         cnt[t] += 1
+                if not ok:
+                    break
                 if j < npos and bug != "early_k_release":
                     commit(k_empty[s])
                 if j >= 1:
                     commit(v_empty[sp])
                 use_prev = use
+                j += 1
+        # every MMA issued by this thread has finished before tensor memory is released
+        commit(mma_done)
+        yield from sim.drain(mma_done, 0)
 
     def softmax(t, q):
         n = nsteps[t]
+        ok = True
         for j in range(n):
-            yield from wait(s_full[t], j & 1, j + 1)
+            ok = yield from wait_ok(s_full[t], j & 1, j + 1)
+            if not ok:
+                break
             Sreg[t][q].read(("S", j), consume=True)
             # rescaling O~ needs every earlier P V of the tile to have completed
             assert O[t] == j, f"O{t}: {O[t]} P V applied at softmax step {j}"
             Sreg[t][q].write(("P", j), readers=1)
             p_full[t].arrive()
-        if n > 0:
-            yield from wait(o_full[t], 0, 1)
-            assert O[t] == n
+        if ok and n > 0:
+            ok = yield from wait_ok(o_full[t], 0, 1)
+            if ok:
+                assert O[t] == n
 
     sim.run([producer()] + [softmax(t, q) for t in range(2) for q in range(4)], mma())
-    for t in range(2):
-        assert done["S"][t] == list(range(nsteps[t])), done
-        assert done["PV"][t] == list(range(nsteps[t])), done
+    assert sim.exit_ops == 0, f"CTA exits with {sim.exit_ops} MMA operations queued"
+    if not sim.abort:
+        assert sim.exit_copies == 0, f"CTA exits with {sim.exit_copies} copies in flight"
+        for t in range(2):
+            assert done["S"][t] == list(range(nsteps[t])), done
+            assert done["PV"][t] == list(range(nsteps[t])), done
+    return sim
 
 
 # ------------------------------------------------------------------------------------------
@@ -324,6 +412,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
     s_full, dp_full = Bar(1, "s_full"), Bar(1, "dp_full")
     p_full, ds_full, dq_empty = Bar(W, "p_full"), Bar(W, "ds_full"), Bar(W, "dq_empty")
     dq_full, dkdv_full = Bar(1, "dq_full"), Bar(1, "dkdv_full")
+    mma_done = Bar(1, "mma_done")
     KV = Buf("KV")
     Qst = [Buf(f"Q{s}") for s in range(2)]
     dOst = [Buf(f"dO{s}") for s in range(2)]
@@ -453,6 +542,8 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
                     yield from wait_q(it + 2)
                     issue_S(it + 2)
         sim.issue(dkdv_full.arrive)
+        sim.issue(mma_done.arrive)
+        yield from sim.drain(mma_done, 0)
 
     def elementwise(c, k):
         def drain(it):
@@ -485,6 +576,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
             assert acc["dV"] == nit and acc["dK"] == nit
 
     sim.run([producer()] + [elementwise(c, k) for k, c in enumerate(cells)], mma())
+    assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
     assert acc == {"dV": nit, "dK": nit}
     if with_dq:
         assert all(d == list(range(nit)) for d in drained)
@@ -509,6 +601,7 @@ def dq_kernel(nb, seed, bug=None):
     dp_full = [Bar(1, f"dp_full{b}") for b in range(2)]
     ds_full = [Bar(W, f"ds_full{b}") for b in range(2)]
     dq_full = Bar(1, "dq_full")
+    mma_done = Bar(1, "mma_done")
     QdO = Buf("QdO")
     Kst = [Buf(f"K{s}") for s in range(2)]
     Vst = [Buf(f"V{s}") for s in range(2)]
@@ -595,6 +688,8 @@ def dq_kernel(nb, seed, bug=None):
             yield from wait(ds_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
             issue_dQ(jj)
         sim.issue(dq_full.arrive)
+        sim.issue(mma_done.arrive)
+        yield from sim.drain(mma_done, 0)
 
     def elementwise(c):
         for jj in range(nb):
@@ -610,4 +705,5 @@ def dq_kernel(nb, seed, bug=None):
             assert acc["dQ"] == nb
 
     sim.run([producer()] + [elementwise(c) for c in cells], mma())
+    assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
     assert acc["dQ"] == nb

@@ -77,3 +77,39 @@ def test_checker_catches_an_early_stage_release(half):
 
 def test_checker_catches_an_overwrite_of_unread_scores():
     assert _fails(lambda seed: dq_kernel(6, seed, bug="s_before_read"))
+
+
+def _abort_runs(half, S, drain_always):
+    """Sims of forward runs in which one wait, at many points of many runs, times out."""
+    import random
+
+    rng = random.Random(11)
+    for n0, n1 in [(1, 1), (3, 4), (6, 8), (7, 7)]:
+        for seed in range(6):
+            spins = forward((n0, n1), S, half, seed, drain_always=drain_always).spins
+            for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
+                yield forward((n0, n1), S, half, seed, abort_at=abort_at,
+                              drain_always=drain_always)
+
+
+@pytest.mark.parametrize("half,S", [(False, 2), (False, 4), (True, 2)],
+                         ids=["128-key-2-stages", "128-key-4-stages", "half-step-2-stages"])
+def test_forward_timeout_every_role_leaves(half, S):
+    """A wait that runs past its limit, at any point of any role: every role leaves (no
+    deadlock) and no MMA is still queued when the CTA exits."""
+    for sim in _abort_runs(half, S, drain_always=False):
+        assert sim.abort and sim.exit_ops == 0
+
+
+def test_forward_timeout_copies_in_flight_at_exit():
+    """Known gap of the kernels' timeout path: the producer waits for its last copies only if
+    the abort flag is already set when it leaves its loop.  If another role times out after
+    that, a copy issued just before can still be in flight when the CTA exits.  Waiting for the
+    last copies unconditionally (drain_always: in a normal run they land within microseconds,
+    while the producer thread would sit at the final barrier anyway) leaves none in any of these
+    interleavings."""
+    current = [sim.exit_copies for sim in _abort_runs(False, 2, drain_always=False)]
+    assert any(c > 0 for c in current)
+    for half, S in [(False, 2), (False, 4), (True, 2)]:
+        for sim in _abort_runs(half, S, drain_always=True):
+            assert sim.exit_copies == 0 and sim.exit_ops == 0
