@@ -395,14 +395,16 @@ def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, drain_alw
 # its share of the query columns of S^T / dP^T and of the dQ columns, per 32-lane quadrant (the
 # d = 128 column layout: a group's dQ columns are its own dS columns).
 
-def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
+def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None):
     """`bug` plants a protocol error (for the tests that show the checker catches it):
     "dv_before_do": dV(i+1) issued before waiting for dO(i+1)'s copy (a race once present in the
     kernel); "early_q_release": Q_i's stage released before dK(i), its last reader.
     ("early_do_release", dO(i+1)'s stage released right after dV(i+1) and before dP(i+1), is
     harmless under this producer order: the producer refills that stage only after Q_(i+3)'s
-    stage, which dK(i+1) releases after dP(i+1) has run; the tests show that too.)"""
-    sim = Sim(seed)
+    stage, which dK(i+1) releases after dP(i+1) has run; the tests show that too.)
+    `abort_at`: as for forward(); the roles then leave as the kernel's do.  Returns the Sim."""
+    sim = Sim(seed, abort_at)
+    wait_ok = sim.wait_ok
     W = 4 * groups  # elementwise warps
     kv_full = Bar(1, "kv_full")
     q_full = [Bar(1, f"q_full{s}") for s in range(2)]
@@ -431,9 +433,11 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
             KV.write("KV")
             kv_full.arrive()
         sim.copy(kv_copy)
+        nq = ndo = 0  # Q and dO copies issued
         for it in range(nit):
             s, ph = it & 1, (it >> 1) & 1
-            yield from wait(q_empty[s], ph ^ 1, it >> 1)
+            if not (yield from wait_ok(q_empty[s], ph ^ 1, it >> 1)):
+                break
 
             # Q_i is read by S(i) and dK(i), its LSE and D rows by every elementwise warp (for
             # P and for dS); dO_i by dP(i) and dV(i)
@@ -441,12 +445,21 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
                 Qst[s].write(it, readers=2 + 2 * W)
                 q_full[s].arrive()
             sim.copy(q_copy)
-            yield from wait(do_empty[s], ph ^ 1, it >> 1)
+            nq = it + 1
+            if not (yield from wait_ok(do_empty[s], ph ^ 1, it >> 1)):
+                break
 
             def do_copy(s=s, it=it):
                 dOst[s].write(it, readers=2)
                 do_full[s].arrive()
             sim.copy(do_copy)
+            ndo = it + 1
+        if sim.abort:
+            yield from sim.drain(kv_full, 0)
+            for i in range(max(0, nq - 2), nq):
+                yield from sim.drain(q_full[i & 1], (i >> 1) & 1)
+            for i in range(max(0, ndo - 2), ndo):
+                yield from sim.drain(do_full[i & 1], (i >> 1) & 1)
 
     def mma():
         if nit == 0:
@@ -505,81 +518,112 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None):
                 sim.issue(dq_full.arrive)
 
         def wait_q(it):
-            yield from wait(q_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)
+            return (yield from wait_ok(q_full[it & 1], (it >> 1) & 1, (it >> 1) + 1))
 
         def wait_do(it):
-            yield from wait(do_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)
+            return (yield from wait_ok(do_full[it & 1], (it >> 1) & 1, (it >> 1) + 1))
 
-        yield from wait(kv_full, 0, 1)
-        yield from wait_q(0)
-        issue_S(0)
-        yield from wait_do(0)
-        issue_dP(0)
-        yield from wait(p_full, 0, 1)
-        issue_dV(0)
-        release_do(0)
-        if nit > 1:
-            yield from wait_q(1)
-            issue_S(1)
-        for it in range(nit):
-            yield from wait(ds_full, it & 1, it + 1)
+        ok = (yield from wait_ok(kv_full, 0, 1)) and (yield from wait_q(0))
+        if ok:
+            issue_S(0)
+            ok = yield from wait_do(0)
+        if ok:
+            issue_dP(0)
+            ok = yield from wait_ok(p_full, 0, 1)
+        if ok:
+            issue_dV(0)
+            release_do(0)
+            if nit > 1:
+                ok = yield from wait_q(1)
+                if ok:
+                    issue_S(1)
+        it = 0
+        while ok and it < nit:
+            ok = yield from wait_ok(ds_full, it & 1, it + 1)
+            if not ok:
+                break
             issue_dK_dQ(it)
             if it + 1 < nit:
-                yield from wait(p_full, (it + 1) & 1, it + 2)
-                if bug != "dv_before_do":
-                    yield from wait_do(it + 1)
+                ok = yield from wait_ok(p_full, (it + 1) & 1, it + 2)
+                if ok and bug != "dv_before_do":
+                    ok = yield from wait_do(it + 1)
+                if not ok:
+                    break
                 issue_dV(it + 1)
                 if bug == "dv_before_do":
-                    yield from wait_do(it + 1)
+                    ok = yield from wait_do(it + 1)
+                    if not ok:
+                        break
                 if bug == "early_do_release":
                     release_do(it + 1)
                 if with_dq:
-                    yield from wait(dq_empty, it & 1, it + 1)
+                    ok = yield from wait_ok(dq_empty, it & 1, it + 1)
+                    if not ok:
+                        break
                 issue_dP(it + 1)
                 if bug != "early_do_release":
                     release_do(it + 1)
                 if it + 2 < nit:
-                    yield from wait_q(it + 2)
+                    ok = yield from wait_q(it + 2)
+                    if not ok:
+                        break
                     issue_S(it + 2)
-        sim.issue(dkdv_full.arrive)
+            it += 1
+        if ok:
+            sim.issue(dkdv_full.arrive)
         sim.issue(mma_done.arrive)
         yield from sim.drain(mma_done, 0)
 
     def elementwise(c, k):
         def drain(it):
-            yield from wait(dq_full, it & 1, it + 1)
+            if not (yield from wait_ok(dq_full, it & 1, it + 1)):
+                return False
             DPreg[c].read(("dQ", it), consume=True)
             drained[k].append(it)
             dq_empty.arrive()
+            return True
 
+        ok = True
         for it in range(nit):
             s, ph = it & 1, (it >> 1) & 1
-            yield from wait(q_full[s], ph, (it >> 1) + 1)
+            ok = yield from wait_ok(q_full[s], ph, (it >> 1) + 1)
+            if not ok:
+                break
             Qst[s].read(it, consume=True)  # the LSE and D rows of this query tile
-            yield from wait(s_full, it & 1, it + 1)
+            ok = yield from wait_ok(s_full, it & 1, it + 1)
+            if not ok:
+                break
             Sreg[c].read(("S", it), consume=True)
             Sreg[c].write(("P", it), readers=1)
             p_full.arrive()
             if with_dq and it > 0:
-                yield from drain(it - 1)
-            yield from wait(dp_full, it & 1, it + 1)
+                ok = yield from drain(it - 1)
+                if not ok:
+                    break
+            ok = yield from wait_ok(dp_full, it & 1, it + 1)
+            if not ok:
+                break
             DPreg[c].read(("dP", it), consume=True)
             Qst[s].read(it, consume=True)
             DPreg[c].write(("dS", it), readers=1)
             if with_dq:
                 DS[c].write(("dS", it), readers=1)
             ds_full.arrive()
-        if with_dq and nit > 0:
-            yield from drain(nit - 1)
-        if nit > 0:
-            yield from wait(dkdv_full, 0, 1)
-            assert acc["dV"] == nit and acc["dK"] == nit
+        if with_dq and ok and nit > 0:
+            ok = yield from drain(nit - 1)
+        if ok and nit > 0:
+            ok = yield from wait_ok(dkdv_full, 0, 1)
+            if ok:
+                assert acc["dV"] == nit and acc["dK"] == nit
 
     sim.run([producer()] + [elementwise(c, k) for k, c in enumerate(cells)], mma())
-    assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
-    assert acc == {"dV": nit, "dK": nit}
-    if with_dq:
-        assert all(d == list(range(nit)) for d in drained)
+    assert sim.exit_ops == 0, f"CTA exits with {sim.exit_ops} MMA operations queued"
+    if not sim.abort:
+        assert sim.exit_copies == 0, f"CTA exits with {sim.exit_copies} copies in flight"
+        assert acc == {"dV": nit, "dK": nit}
+        if with_dq:
+            assert all(d == list(range(nit)) for d in drained)
+    return sim
 
 
 # ------------------------------------------------------------------------------------------

@@ -113,3 +113,18 @@ def test_forward_timeout_copies_in_flight_at_exit():
     for half, S in [(False, 2), (False, 4), (True, 2)]:
         for sim in _abort_runs(half, S, drain_always=True):
             assert sim.exit_copies == 0 and sim.exit_ops == 0
+
+
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_dkdv_timeout_every_role_leaves(with_dq):
+    """The dK/dV kernel's timeout path: a wait runs out at any point of any role; every role
+    leaves and no MMA is still queued when the CTA exits."""
+    import random
+
+    rng = random.Random(13)
+    for nit in (1, 2, 5, 8):
+        for seed in range(5):
+            spins = dkdv(nit, seed, with_dq=with_dq).spins
+            for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
+                sim = dkdv(nit, seed, with_dq=with_dq, abort_at=abort_at)
+                assert sim.abort and sim.exit_ops == 0
