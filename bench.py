@@ -410,13 +410,14 @@ def host_link_gbs(h_in, h_out, stream, reps=3):
 
 
 # ------------------------------------------------------------------------------- arms
-def workload_config(w, extra, args, world, l2):
+def workload_config(w, extra, args, world):
     """The line's `config`: the workload's name and shape; `extra` is kv_lens (dense, may be
-    None) or cu_seqlens (variable-length)."""
+    None) or cu_seqlens (variable-length).  Both arms print the same object for the same
+    arguments; how each arm treats L2 is a key of its own beside it."""
     varlen = w.seqlen_range is not None
     kv = None if varlen else extra
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-            "kv_lens": None if kv is None else kv.tolist(), "l2": l2,
+            "kv_lens": None if kv is None else kv.tolist(),
             "parallelism": f"replicas x{world}", "bwd": args.bwd, "block_mask": w.block_mask,
             "Hkv": w.kv_heads, "seqlens": extra.diff().tolist() if varlen else None}
 
@@ -439,7 +440,8 @@ def run_reference(args, w, world, rank):
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, kv, args, world, l2="n/a (CPU oracle)"),
+        "config": workload_config(w, kv, args, world),
+        "l2": "n/a (CPU oracle)",
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample,
                          "full_step_seconds_extrapolated": sum(w.flops()) / (value * 1e12)},
@@ -610,16 +612,19 @@ def run_ours(args, w, world, rank, local):
         link = host_link_gbs(hq, hout["O"], stream)
         barrier(world)
         torch.cuda.synchronize()
-        a, bv = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
+        # one event per replay boundary: the total and each replay's own duration
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        marks[0].record(stream)
+        for i in range(args.steps):
             e2e_step()
-        bv.record(stream)
+            marks[i + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        e2e_ms = max_over_ranks(a.elapsed_time(bv), world) / args.steps
+        per = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
+        e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world) / args.steps
         e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "replay_ms": {"median": statistics.median(per), "min": min(per), "max": max(per)},
                "chunks": len(ha.plan), "host_link_gbs": link}
         assert fa.fa_get_error() == fa.FA_OK
 
@@ -650,19 +655,29 @@ def run_ours(args, w, world, rank, local):
 
     fwd_tf = f_fwd / (stage_ms["fwd"] * 1e-3) / 1e12
     bwd_ms = sum(stage_ms[s] for s in stages[1:])
+    effective = None
+    if w.kv_len_range is not None:  # the work the kernels do: only the visible (query, key) pairs
+        e_fwd, e_bwd = w.flops_effective(kv)
+        effective = {"note": "FLOPs of the visible (query, key) pairs, N * len_b per head",
+                     "tflops": (e_fwd + e_bwd) * world / (ms_step * 1e-3) / 1e12,
+                     "fwd_tflops": e_fwd / (stage_ms["fwd"] * 1e-3) / 1e12,
+                     "bwd_tflops": e_bwd / (bwd_ms * 1e-3) / 1e12,
+                     "fraction_of_nominal": (e_fwd + e_bwd) / (f_fwd + f_bwd)}
+        effective["fwd_frac_of_peak"] = effective["fwd_tflops"] / peak
+        effective["bwd_frac_of_peak"] = effective["bwd_tflops"] / peak
     line = {
         "metric": METRIC,
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(
-            w, extra, args, world,
-            l2=("flushed: 256 MB written between steps, outside the per-step events summed"
-                if in_l2 else "inputs larger than L2 (no flush)")),
+        "config": workload_config(w, extra, args, world),
+        "l2": ("flushed: 256 MB written between steps, outside the per-step events summed"
+               if in_l2 else "inputs larger than L2 (no flush)"),
         "fwd_tflops": fwd_tf, "fwd_frac_of_peak": fwd_tf / peak,
         "bwd_tflops": f_bwd / (bwd_ms * 1e-3) / 1e12,
         "bwd_frac_of_peak": f_bwd / (bwd_ms * 1e-3) / 1e12 / peak,
         "stage_ms": stage_ms,
+        "effective": effective,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

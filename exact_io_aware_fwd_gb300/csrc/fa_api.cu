@@ -30,16 +30,22 @@ int* status_ptr() {
   return static_cast<int*>(p);
 }
 
+// Limit of a single pipeline wait in the kernels, read at every call so that a process can
+// change it between calls: FA_WAIT_TIMEOUT_US (microseconds) if set to a positive value, else
+// FA_WAIT_TIMEOUT_MS (milliseconds), else 2 s.  A wait is normally a few microseconds; a limit
+// below that makes a normal launch give up with FA_ERR_TIMEOUT, which is how the kernels' timeout
+// paths are exercised without a fault.  (The waits a CTA makes for its own copies and MMAs before
+// it exits keep a limit of at least 1 s, whatever this is.)
 uint64_t wait_timeout_ns() {
-  static const uint64_t ns = [] {  // initialised once, thread-safely
-    uint64_t ms = 2000;  // a single pipeline wait is normally a few microseconds
-    if (const char* e = std::getenv("FA_WAIT_TIMEOUT_MS")) {
-      const long v = std::strtol(e, nullptr, 10);
-      if (v > 0) ms = static_cast<uint64_t>(v);
-    }
-    return ms * 1000000ull;
-  }();
-  return ns;
+  if (const char* e = std::getenv("FA_WAIT_TIMEOUT_US")) {
+    const long long v = std::strtoll(e, nullptr, 10);
+    if (v > 0) return static_cast<uint64_t>(v) * 1000ull;
+  }
+  if (const char* e = std::getenv("FA_WAIT_TIMEOUT_MS")) {
+    const long long v = std::strtoll(e, nullptr, 10);
+    if (v > 0) return static_cast<uint64_t>(v) * 1000000ull;
+  }
+  return 2000ull * 1000000ull;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

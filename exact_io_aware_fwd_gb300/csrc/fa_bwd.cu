@@ -57,17 +57,6 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > c.timeout_ns) {
-      ctl_fail(c, kErrTimeout);
-      return;
-    }
-  }
-}
-
 // Row geometry of the preprocess and dQ-conversion kernels.  Dense: block (i, bh) is query tile i
 // of head slice bh of [B*H, N, d].  Variable-length: block (i, b*H + h) is tile i of sequence b,
 // head h of the packed [total, H, d] tensors, whose workspace tile is h * ws_tiles + tile0 + i.
@@ -377,12 +366,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                       q_y(h, i * 128), q_z(h, i * 128));
         ndo = it + 1;
       }
-      if (*abort_flag) {
-        drain_wait(kv_full, 0, ctl);
-        for (int it = max(0, nq - 2); it < nq; ++it) drain_wait(&q_full[it & 1], (it >> 1) & 1, ctl);
-        for (int it = max(0, ndo - 2); it < ndo; ++it)
-          drain_wait(&do_full[it & 1], (it >> 1) & 1, ctl);
-      }
+      // no copy may still be in flight when the CTA exits, aborted or not
+      drain_wait(kv_full, 0, ctl);
+      for (int it = max(0, nq - 2); it < nq; ++it) drain_wait(&q_full[it & 1], (it >> 1) & 1, ctl);
+      for (int it = max(0, ndo - 2); it < ndo; ++it)
+        drain_wait(&do_full[it & 1], (it >> 1) & 1, ctl);
     }
   } else if (warp == 1) {
     // ================= MMA issuer

@@ -27,17 +27,6 @@ namespace fa {
 
 namespace {
 
-__device__ __forceinline__ void drain_wait_dq(uint64_t* bar, uint32_t parity, const Ctl& c) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > c.timeout_ns) {
-      ctl_fail(c, kErrTimeout);
-      return;
-    }
-  }
-}
-
 template <int D>
 struct DqLayout {
   static constexpr uint32_t kTile = 128u * D * 2u;
@@ -192,11 +181,10 @@ __global__ void __launch_bounds__(384, 1)
                       kv_z(kt));
         nv = jj + 1;
       }
-      if (*abort_flag) {
-        drain_wait_dq(qdo_full, 0, ctl);
-        for (int jj = max(0, nk - 2); jj < nk; ++jj) drain_wait_dq(&k_full[jj & 1], (jj >> 1) & 1, ctl);
-        for (int jj = max(0, nv - 2); jj < nv; ++jj) drain_wait_dq(&v_full[jj & 1], (jj >> 1) & 1, ctl);
-      }
+      // no copy may still be in flight when the CTA exits, aborted or not
+      drain_wait(qdo_full, 0, ctl);
+      for (int jj = max(0, nk - 2); jj < nk; ++jj) drain_wait(&k_full[jj & 1], (jj >> 1) & 1, ctl);
+      for (int jj = max(0, nv - 2); jj < nv; ++jj) drain_wait(&v_full[jj & 1], (jj >> 1) & 1, ctl);
     }
   } else if (warp == 1) {
     // ================= MMA issuer: S(0), dP(0), then per key tile j:
@@ -250,7 +238,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (ok) mma_commit(dq_full);
       mma_commit(mma_done);
-      drain_wait_dq(mma_done, 0, ctl);
+      drain_wait(mma_done, 0, ctl);
     }
   } else if (warp >= 4) {
     // ================= P and dS: one thread per query row, one warpgroup per 64 keys

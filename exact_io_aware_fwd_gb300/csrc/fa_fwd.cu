@@ -131,19 +131,6 @@ struct FwdLayout {
   static constexpr uint32_t kTmemCols = kHalf ? 256 : 512;
 };
 
-// Wait that ignores the abort flag (used only to drain this CTA's own asynchronous work
-// before exit); bounded by the same time limit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
-  const uint32_t a = smem_u32(bar);
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(a, parity)) {
-    if (globaltimer_ns() - t0 > c.timeout_ns) {
-      ctl_fail(c, kErrTimeout);
-      return;
-    }
-  }
-}
-
 // Number of entries of the ascending list[0, cnt) below lim (whole warp; a sorted list fails the
 // test only after its last passing entry).
 __device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, int lim) {
@@ -321,12 +308,12 @@ __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
                       row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
         jv = j + 1;
       }
-      if (*abort_flag) {
-        // no copy into this CTA's shared memory may still be in flight when the CTA exits
-        drain_wait(q_full, 0, ctl);
-        for (int jj = max(0, jk - S); jj < jk; ++jj) drain_wait(&k_full[jj % S], (jj / S) & 1, ctl);
-        for (int jj = max(0, jv - S); jj < jv; ++jj) drain_wait(&v_full[jj % S], (jj / S) & 1, ctl);
-      }
+      // No copy into this CTA's shared memory may still be in flight when the CTA exits, whether
+      // or not any role has aborted (one may time out after this thread left its loop).  In a
+      // normal run the consumers have already waited for these phases.
+      drain_wait(q_full, 0, ctl);
+      for (int jj = max(0, jk - S); jj < jk; ++jj) drain_wait(&k_full[jj % S], (jj / S) & 1, ctl);
+      for (int jj = max(0, jv - S); jj < jv; ++jj) drain_wait(&v_full[jj % S], (jj / S) & 1, ctl);
     }
   } else if (warp == 1) {
     // ================= MMA issuer

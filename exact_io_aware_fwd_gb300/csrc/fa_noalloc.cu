@@ -34,7 +34,20 @@ static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchByte
 
 constexpr int kMaxDevices = 64;
 
-// Device address of g_bwd_scratch on the current device, looked up once per device.
+// The library's kernels are built for compute capability 10.3 only; on any other GPU the array
+// has no device image either, so the call is refused before the address lookup.
+fa_status check_device_cc() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return (major == 10 && minor == 3) ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// Device address of g_bwd_scratch on the current device, looked up once per device.  A failed
+// lookup is cleared from the runtime's last-error state, so that it is not reported again by a
+// later, unrelated call.
 void* scratch_address() {
   static void* addr[kMaxDevices] = {nullptr};
   static std::mutex mu;
@@ -43,7 +56,10 @@ void* scratch_address() {
   std::lock_guard<std::mutex> lock(mu);
   if (addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
     addr[dev] = p;
   }
   return addr[dev];
@@ -62,6 +78,8 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
   const size_t need = fa_bwd_workspace_size(B, H, N, d);
   if (need == 0) return FA_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return FA_ERR_WORKSPACE;  // larger than the static array
+  const fa_status dev_ok = check_device_cc();
+  if (dev_ok != FA_OK) return dev_ok;
   void* ws = scratch_address();
   if (ws == nullptr) return FA_ERR_CUDA;
   return fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, d, causal, scale, kv_lens, ws,

@@ -91,6 +91,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   }
 }
 
+// Wait that ignores the abort flag, used only to drain this CTA's own asynchronous work (the
+// copies and MMAs it issued) before it exits: a copy still in flight at exit would land in the
+// shared memory of the next CTA on the SM.  Such work completes within microseconds whatever
+// happened to the pipeline, so the limit never falls below kDrainLimitNs, however short the
+// pipeline limit is; it only ends a wait on a memory system that has stopped answering.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // 1 s
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const Ctl& c) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t limit = c.timeout_ns > kDrainLimitNs ? c.timeout_ns : kDrainLimitNs;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > limit) {
+      ctl_fail(c, kErrTimeout);
+      return;
+    }
+  }
+}
+
 // Whole-warp variant: every lane waits, and the warp agrees on the outcome so that the
 // .sync.aligned instructions that follow are executed by all lanes or by none.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Ctl& c) {

@@ -81,6 +81,23 @@ class Workload:
             f, b = f / 2, b / 2
         return f, b
 
+    def flops_effective(self, kv_lens) -> tuple[float, float]:
+        """(forward, backward) FLOPs of the (query, key) pairs a key-padded workload actually
+        keeps, given its drawn key lengths (workload_inputs' last item): 4 d and 10 d per visible
+        pair, N * len_b pairs per head of batch b (causal: the pairs with key <= query among the
+        first len_b keys).  The kernels skip the key tiles at or past len_b, so this, not the
+        nominal N^2 count, is the work they do.  Without key lengths: flops()."""
+        if kv_lens is None or self.kv_len_range is None:
+            return self.flops()
+        lens = torch.as_tensor(kv_lens).double().clamp(0, self.N)
+        n = float(self.N)
+        if self.causal:  # sum over queries i of min(i + 1, len_b)
+            pairs = lens * (lens + 1) / 2 + (n - lens) * lens
+        else:
+            pairs = n * lens
+        per_head_sum = float(pairs.sum()) * self.d  # summed over the batch
+        return 4.0 * per_head_sum * self.H, 10.0 * per_head_sum * self.H
+
 
 # The five synthetic shapes: a one-head smoke test, the GPT-2-medium attention shape the pages
 # time on A100, a causal mid-length case, the long-context causal case the roofline is quoted

@@ -168,15 +168,16 @@ class Sim:
 # Forward kernel (dense, one CTA = two 128-row query tiles).  nsteps[t]: key steps of query tile
 # t (128-key tiles, or 64-key half steps when half=True); S: K/V ring stages.
 
-def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, drain_always=False):
+def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, conditional_drain=False):
     """`bug` = "early_k_release" plants a known protocol error: each K stage is released before
     the S MMAs of its step (or half step) have been issued.  `uses` (block-sparse, 128-key steps):
     per position of the K/V stream a nonzero bit mask of the query tiles that keep that key tile;
     nsteps is then derived from it.  `abort_at`: the abort_at-th spin of any bounded wait runs
     past its time limit (the kernel's timeout path); every role must then leave, with no MMA
-    queued.  `drain_always`: the producer waits for its last copies whether or not the CTA has
-    aborted (the kernel waits only when the abort flag is already set as its producer leaves its
-    loop; see test_pipeline_protocols.py).  Returns the Sim (its spin count, exit state)."""
+    queued.  As in the kernel, the producer then waits for its last copies whether or not the CTA
+    has aborted; `conditional_drain` plants the earlier form, which waited only when the abort flag
+    was already set as the producer left its loop (see test_pipeline_protocols.py).  Returns the
+    Sim (its spin count, exit state)."""
     if uses is not None:
         assert not half and all(u in (1, 2, 3) for u in uses)
         nsteps = (sum(u & 1 for u in uses), sum((u >> 1) & 1 for u in uses))
@@ -239,7 +240,7 @@ def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, drain_alw
                 break
             load(Vst[s], j, readers_of(j), v_full[s])
             jv = j + 1
-        if sim.abort or drain_always:
+        if sim.abort or not conditional_drain:
             # no copy into this CTA's shared memory may still be in flight when it exits
             yield from sim.drain(q_full, 0)
             for jj in range(max(0, jk - S), jk):
@@ -395,14 +396,15 @@ def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, drain_alw
 # its share of the query columns of S^T / dP^T and of the dQ columns, per 32-lane quadrant (the
 # d = 128 column layout: a group's dQ columns are its own dS columns).
 
-def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None):
+def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional_drain=False):
     """`bug` plants a protocol error (for the tests that show the checker catches it):
     "dv_before_do": dV(i+1) issued before waiting for dO(i+1)'s copy (a race once present in the
     kernel); "early_q_release": Q_i's stage released before dK(i), its last reader.
     ("early_do_release", dO(i+1)'s stage released right after dV(i+1) and before dP(i+1), is
     harmless under this producer order: the producer refills that stage only after Q_(i+3)'s
     stage, which dK(i+1) releases after dP(i+1) has run; the tests show that too.)
-    `abort_at`: as for forward(); the roles then leave as the kernel's do.  Returns the Sim."""
+    `abort_at`, `conditional_drain`: as for forward(); the roles then leave as the kernel's do.
+    Returns the Sim."""
     sim = Sim(seed, abort_at)
     wait_ok = sim.wait_ok
     W = 4 * groups  # elementwise warps
@@ -454,7 +456,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None):
                 do_full[s].arrive()
             sim.copy(do_copy)
             ndo = it + 1
-        if sim.abort:
+        if sim.abort or not conditional_drain:
             yield from sim.drain(kv_full, 0)
             for i in range(max(0, nq - 2), nq):
                 yield from sim.drain(q_full[i & 1], (i >> 1) & 1)
@@ -631,10 +633,12 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None):
 # once, K_j and V_j through two stages each; S in one tensor-memory region, dP (then dS) in two
 # alternating ones; two warpgroups of 64 keys each.
 
-def dq_kernel(nb, seed, bug=None):
+def dq_kernel(nb, seed, bug=None, abort_at=None, conditional_drain=False):
     """`bug` = "s_before_read" plants a protocol error: S(j+1) issued without waiting for the
-    warps to have read S(j)."""
-    sim = Sim(seed)
+    warps to have read S(j).  `abort_at`, `conditional_drain`: as for forward(); the roles then
+    leave as the kernel's do.  Returns the Sim."""
+    sim = Sim(seed, abort_at)
+    wait_ok = sim.wait_ok
     W = 8
     qdo_full = Bar(1, "qdo_full")
     k_full = [Bar(1, f"k_full{s}") for s in range(2)]
@@ -662,20 +666,31 @@ def dq_kernel(nb, seed, bug=None):
             QdO.write("QdO")
             qdo_full.arrive()
         sim.copy(qdo)
+        nk = nv = 0
         for jj in range(nb):
             s, ph = jj & 1, (jj >> 1) & 1
-            yield from wait(k_empty[s], ph ^ 1, jj >> 1)
+            if not (yield from wait_ok(k_empty[s], ph ^ 1, jj >> 1)):
+                break
 
             def k_copy(s=s, jj=jj):
                 Kst[s].write(jj, readers=2)  # S(j) and dQ(j)
                 k_full[s].arrive()
             sim.copy(k_copy)
-            yield from wait(v_empty[s], ph ^ 1, jj >> 1)
+            nk = jj + 1
+            if not (yield from wait_ok(v_empty[s], ph ^ 1, jj >> 1)):
+                break
 
             def v_copy(s=s, jj=jj):
                 Vst[s].write(jj, readers=1)  # dP(j)
                 v_full[s].arrive()
             sim.copy(v_copy)
+            nv = jj + 1
+        if sim.abort or not conditional_drain:
+            yield from sim.drain(qdo_full, 0)
+            for jj in range(max(0, nk - 2), nk):
+                yield from sim.drain(k_full[jj & 1], (jj >> 1) & 1)
+            for jj in range(max(0, nv - 2), nv):
+                yield from sim.drain(v_full[jj & 1], (jj >> 1) & 1)
 
     def mma():
         if nb == 0:
@@ -711,43 +726,56 @@ def dq_kernel(nb, seed, bug=None):
             sim.issue(k_empty[jj & 1].arrive)
 
         def wait_k(jj):
-            yield from wait(k_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            return (yield from wait_ok(k_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1))
 
         def wait_v(jj):
-            yield from wait(v_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            return (yield from wait_ok(v_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1))
 
-        yield from wait(qdo_full, 0, 1)
-        yield from wait_k(0)
-        issue_S(0)
-        yield from wait_v(0)
-        issue_dP(0)
+        ok = (yield from wait_ok(qdo_full, 0, 1)) and (yield from wait_k(0))
+        if ok:
+            issue_S(0)
+            ok = yield from wait_v(0)
+        if ok:
+            issue_dP(0)
         for jj in range(nb):
+            if not ok:
+                break
             if jj + 1 < nb:
                 if bug != "s_before_read":
-                    yield from wait(s_read, jj & 1, jj + 1)
-                yield from wait_k(jj + 1)
+                    ok = yield from wait_ok(s_read, jj & 1, jj + 1)
+                ok = ok and (yield from wait_k(jj + 1))
+                if not ok:
+                    break
                 issue_S(jj + 1)
-                yield from wait_v(jj + 1)
+                if not (ok := (yield from wait_v(jj + 1))):
+                    break
                 issue_dP(jj + 1)
-            yield from wait(ds_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            if not (ok := (yield from wait_ok(ds_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1))):
+                break
             issue_dQ(jj)
-        sim.issue(dq_full.arrive)
+        if ok:
+            sim.issue(dq_full.arrive)
         sim.issue(mma_done.arrive)
         yield from sim.drain(mma_done, 0)
 
     def elementwise(c):
+        ok = True
         for jj in range(nb):
-            yield from wait(s_full, jj & 1, jj + 1)
+            if not (ok := (yield from wait_ok(s_full, jj & 1, jj + 1))):
+                break
             Sreg[c].read(("S", jj), consume=True)
             s_read.arrive()
-            yield from wait(dp_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1)
+            if not (ok := (yield from wait_ok(dp_full[jj & 1], (jj >> 1) & 1, (jj >> 1) + 1))):
+                break
             DPreg[jj & 1][c].read(("dP", jj), consume=True)
             DPreg[jj & 1][c].write(("dS", jj), readers=1)
             ds_full[jj & 1].arrive()
-        if nb > 0:
-            yield from wait(dq_full, 0, 1)
-            assert acc["dQ"] == nb
+        if ok and nb > 0:
+            if (yield from wait_ok(dq_full, 0, 1)):
+                assert acc["dQ"] == nb
 
     sim.run([producer()] + [elementwise(c) for c in cells], mma())
-    assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
-    assert acc["dQ"] == nb
+    if not sim.abort:
+        assert acc["dQ"] == nb
+        assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
+    return sim

@@ -25,9 +25,20 @@ def test_reference_arm_two_ranks_gloo():
     assert d["cpu_baseline"]["full_step_seconds_extrapolated"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["n_gpus"] == 2 and d["config"]["parallelism"] == "replicas x2"
-    # the same config keys as the CUDA arm's line
-    assert set(d["config"]) == {"workload", "B", "H", "N", "d", "causal", "kv_lens", "l2",
-                                "parallelism", "bwd", "block_mask", "Hkv", "seqlens"}
+    # the same config object as the CUDA arm's line for these arguments (both arms build it with
+    # bench.workload_config); how the arm treats L2 is a key of its own, outside config
+    import argparse
+    import importlib.util
+
+    from exact_io_aware_fwd_gb300.workloads import BY_NAME, workload_inputs
+
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    w = BY_NAME["smoke-1x1x128x64"]
+    extra = workload_inputs(w)[4]
+    assert d["config"] == bench.workload_config(w, extra, argparse.Namespace(bwd="atomic"), 2)
+    assert "l2" not in d["config"] and d["l2"]
 
 
 def test_max_over_ranks_gloo(tmp_path):

@@ -1,10 +1,14 @@
-"""Failure detection without a GPU fault: a bounded pipeline wait that runs out.
+"""Failure detection without a GPU fault: bounded pipeline waits that run out.
 
-The library's kernels bound every mbarrier wait (sm103.cuh, mbar_wait).  A test-only kernel built
-from tests/csrc/ waits on an mbarrier that nothing arrives on: the wait must give up after its
-limit, record the timeout code (FA_ERR_TIMEOUT = 4) in the status word, make the CTA's other
-role give up through the shared abort flag, and return normally, after which the GPU runs the
-library as before.
+The library's kernels bound every mbarrier wait (sm103.cuh, mbar_wait).  Two forms:
+  * a test-only kernel built from tests/csrc/ waits on an mbarrier that nothing arrives on: the
+    wait must give up after its limit, record the timeout code (FA_ERR_TIMEOUT = 4) in the status
+    word, make the CTA's other role give up through the shared abort flag, and return normally;
+  * the library's own kernels run with a wait limit of one microsecond, shorter than the normal
+    waits of their pipelines, so that waits run out at whatever point they happen to: every CTA
+    must leave through its timeout path (waiting for its own copies and MMAs before it exits),
+    the call must report FA_ERR_TIMEOUT, and the next call in the same context, with the normal
+    limit, must match the oracle.
 """
 
 import ctypes
@@ -17,6 +21,8 @@ import torch
 
 import exact_io_aware_fwd_gb300 as fa
 from exact_io_aware_fwd_gb300 import build_lib
+from exact_io_aware_fwd_gb300.workloads import make_inputs
+from parity import check_case
 
 pytestmark = pytest.mark.gpu
 
@@ -60,3 +66,31 @@ def test_dead_wait_times_out_and_context_survives(selftest_lib):
     ref = torch.nn.functional.scaled_dot_product_attention(q.float(), q.float(), q.float(),
                                                            is_causal=True)
     assert torch.max(torch.abs(o.float() - ref)) < 2e-2
+
+
+@pytest.mark.parametrize("entry,d,causal", [("fwd", 128, True), ("fwd", 64, False),
+                                            ("bwd", 128, True), ("bwd", 64, False),
+                                            ("bwd_deterministic", 128, True)])
+def test_library_kernels_time_out_then_recover(entry, d, causal, monkeypatch):
+    B, H, N = 1, 2, 1000
+    q, k, v, do, _ = make_inputs(B, H, N, d, seed=41)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd(qd, kd, vd, causal=causal)
+    assert fa.fa_get_error() == fa.FA_OK
+    monkeypatch.setenv("FA_WAIT_TIMEOUT_US", "1")
+    t0 = time.time()
+    if entry == "fwd":
+        fa.fa_fwd(qd, kd, vd, causal=causal)
+    elif entry == "bwd":
+        fa.fa_bwd(qd, kd, vd, o, dod, lse, causal=causal)
+    else:
+        fa.fa_bwd_deterministic(qd, kd, vd, o, dod, lse, causal=causal)
+    st = fa.fa_get_error()
+    wall = time.time() - t0
+    monkeypatch.delenv("FA_WAIT_TIMEOUT_US")
+    assert st == fa.FA_ERR_TIMEOUT, fa.fa_status_string(st)
+    assert wall < 10.0
+    # the same context, the normal limit: every output matches the oracle again
+    check_case(q, k, v, do, causal, None, None, label=f"after {entry} timeout",
+               deterministic=(entry == "bwd_deterministic"))

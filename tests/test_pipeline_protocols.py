@@ -79,46 +79,40 @@ def test_checker_catches_an_overwrite_of_unread_scores():
     assert _fails(lambda seed: dq_kernel(6, seed, bug="s_before_read"))
 
 
-def _abort_runs(half, S, drain_always):
+def _abort_runs(half, S, conditional_drain=False):
     """Sims of forward runs in which one wait, at many points of many runs, times out."""
     import random
 
     rng = random.Random(11)
     for n0, n1 in [(1, 1), (3, 4), (6, 8), (7, 7)]:
         for seed in range(6):
-            spins = forward((n0, n1), S, half, seed, drain_always=drain_always).spins
+            spins = forward((n0, n1), S, half, seed).spins
             for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
                 yield forward((n0, n1), S, half, seed, abort_at=abort_at,
-                              drain_always=drain_always)
+                              conditional_drain=conditional_drain)
 
 
 @pytest.mark.parametrize("half,S", [(False, 2), (False, 4), (True, 2)],
                          ids=["128-key-2-stages", "128-key-4-stages", "half-step-2-stages"])
 def test_forward_timeout_every_role_leaves(half, S):
     """A wait that runs past its limit, at any point of any role: every role leaves (no
-    deadlock) and no MMA is still queued when the CTA exits."""
-    for sim in _abort_runs(half, S, drain_always=False):
-        assert sim.abort and sim.exit_ops == 0
+    deadlock), and when the CTA exits no MMA is queued and no copy is in flight (the producer
+    waits for its last copies whether or not the CTA has aborted)."""
+    for sim in _abort_runs(half, S):
+        assert sim.abort and sim.exit_ops == 0 and sim.exit_copies == 0
 
 
-def test_forward_timeout_copies_in_flight_at_exit():
-    """Known gap of the kernels' timeout path: the producer waits for its last copies only if
-    the abort flag is already set when it leaves its loop.  If another role times out after
-    that, a copy issued just before can still be in flight when the CTA exits.  Waiting for the
-    last copies unconditionally (drain_always: in a normal run they land within microseconds,
-    while the producer thread would sit at the final barrier anyway) leaves none in any of these
-    interleavings."""
-    current = [sim.exit_copies for sim in _abort_runs(False, 2, drain_always=False)]
-    assert any(c > 0 for c in current)
-    for half, S in [(False, 2), (False, 4), (True, 2)]:
-        for sim in _abort_runs(half, S, drain_always=True):
-            assert sim.exit_copies == 0 and sim.exit_ops == 0
+def test_checker_catches_a_drain_only_when_already_aborted():
+    """The kernels' producers once waited for their last copies only if the abort flag was
+    already set when they left their loop; if another role timed out after that, a copy issued
+    just before could still be in flight when the CTA exited and land in the shared memory of
+    the SM's next CTA.  The checker finds that form in all three kernels."""
+    assert any(sim.exit_copies > 0 for sim in _abort_runs(False, 2, conditional_drain=True))
+    assert any(sim.exit_copies > 0 for sim in _dkdv_abort_runs(True, conditional_drain=True))
+    assert any(sim.exit_copies > 0 for sim in _dq_abort_runs(conditional_drain=True))
 
 
-@pytest.mark.parametrize("with_dq", [True, False])
-def test_dkdv_timeout_every_role_leaves(with_dq):
-    """The dK/dV kernel's timeout path: a wait runs out at any point of any role; every role
-    leaves and no MMA is still queued when the CTA exits."""
+def _dkdv_abort_runs(with_dq, conditional_drain=False):
     import random
 
     rng = random.Random(13)
@@ -126,5 +120,30 @@ def test_dkdv_timeout_every_role_leaves(with_dq):
         for seed in range(5):
             spins = dkdv(nit, seed, with_dq=with_dq).spins
             for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
-                sim = dkdv(nit, seed, with_dq=with_dq, abort_at=abort_at)
-                assert sim.abort and sim.exit_ops == 0
+                yield dkdv(nit, seed, with_dq=with_dq, abort_at=abort_at,
+                           conditional_drain=conditional_drain)
+
+
+def _dq_abort_runs(conditional_drain=False):
+    import random
+
+    rng = random.Random(17)
+    for nb in (1, 2, 5, 8):
+        for seed in range(5):
+            spins = dq_kernel(nb, seed).spins
+            for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
+                yield dq_kernel(nb, seed, abort_at=abort_at, conditional_drain=conditional_drain)
+
+
+@pytest.mark.parametrize("with_dq", [True, False])
+def test_dkdv_timeout_every_role_leaves(with_dq):
+    """The dK/dV kernel's timeout path: a wait runs out at any point of any role; every role
+    leaves, and the CTA exits with no MMA queued and no copy in flight."""
+    for sim in _dkdv_abort_runs(with_dq):
+        assert sim.abort and sim.exit_ops == 0 and sim.exit_copies == 0
+
+
+def test_deterministic_dq_timeout_every_role_leaves():
+    """The same for the deterministic dQ kernel."""
+    for sim in _dq_abort_runs():
+        assert sim.abort and sim.exit_ops == 0 and sim.exit_copies == 0
