@@ -267,6 +267,7 @@ fa_status bwd_setup(BwdSetup& st, const Problem& p, const void* Q, const void* K
   a.neg_lse2 = reinterpret_cast<const float*>(ws + w.neg_lse2_off);
   a.neg_delta = reinterpret_cast<const float*>(ws + w.neg_delta_off);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
+  a.dq_cnt = reinterpret_cast<fa::DqTileCount*>(ws + w.dq_cnt_off);
   a.blk = p.blk;
   a.blk_heads = p.blk_heads;
   a.status = status;
@@ -275,9 +276,9 @@ fa_status bwd_setup(BwdSetup& st, const Problem& p, const void* Q, const void* K
   return FA_OK;
 }
 
-// Every fused backward entry point: preprocess, then either the dK/dV kernel with dQ atomics and
-// the dQ conversion, or (deterministic) the dK/dV kernel without dQ and the per-query-tile dQ
-// kernel.
+// Every fused backward entry point: preprocess, then either the dK/dV kernel with the dQ
+// accumulation and the dQ conversion, or (deterministic) the dK/dV kernel without dQ and the
+// per-query-tile dQ kernel.
 fa_status bwd_impl(const Problem& p, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
                    void* workspace, size_t workspace_bytes, bool deterministic, void* stream) {
@@ -293,14 +294,16 @@ fa_status bwd_impl(const Problem& p, const void* Q, const void* K, const void* V
   float* neg_lse2 = reinterpret_cast<float*>(ws + w.neg_lse2_off);
   float* neg_delta = reinterpret_cast<float*>(ws + w.neg_delta_off);
   float* acc = reinterpret_cast<float*>(ws + w.dq_acc_off);
+  fa::DqTileCount* recs = reinterpret_cast<fa::DqTileCount*>(ws + w.dq_cnt_off);
+  fa::DqTileCount* reset = deterministic ? nullptr : recs;  // the deterministic path has none
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int max_tiles = (p.N + 127) / 128;
   cudaError_t e =
       p.varlen() ? fa::launch_bwd_preprocess_varlen(p.d, O, dO, LSE, p.cu_seqlens, p.B, p.H,
                                                     max_tiles, p.total, p.ws_tiles(), neg_lse2,
-                                                    neg_delta, acc, !deterministic, s)
+                                                    neg_delta, reset, s)
                  : fa::launch_bwd_preprocess(p.d, O, dO, LSE, p.B * p.H, p.N, neg_lse2, neg_delta,
-                                             acc, !deterministic, s);
+                                             reset, s);
   if (e == cudaSuccess)
     e = fa::launch_bwd_dkdv(p.d, /*with_dq=*/!deterministic, st.tq, st.tk, st.tv, st.tdo, st.tdk,
                             st.tdv, st.a, s);
@@ -308,10 +311,10 @@ fa_status bwd_impl(const Problem& p, const void* Q, const void* K, const void* V
     if (deterministic)
       e = fa::launch_bwd_dq(p.d, st.tq, st.tk, st.tv, st.tdo, st.tdq, st.a, s);
     else if (p.varlen())
-      e = fa::launch_bwd_dq_convert_varlen(p.d, acc, dQ, p.cu_seqlens, p.B, p.H, max_tiles,
-                                           p.total, p.ws_tiles(), st.a.scale, s);
+      e = fa::launch_bwd_dq_convert_varlen(p.d, acc, recs, dQ, p.cu_seqlens, p.B, p.H,
+                                           max_tiles, p.total, p.ws_tiles(), st.a.scale, s);
     else
-      e = fa::launch_bwd_dq_convert(p.d, acc, dQ, p.B * p.H, p.N, st.a.scale, s);
+      e = fa::launch_bwd_dq_convert(p.d, acc, recs, dQ, p.B * p.H, p.N, st.a.scale, s);
   }
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -427,8 +430,8 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE, int
   char* ws = static_cast<char*>(workspace);
   cudaError_t e = fa::launch_bwd_preprocess(
       d, O, dO, LSE, BH, N, reinterpret_cast<float*>(ws + w.neg_lse2_off),
-      reinterpret_cast<float*>(ws + w.neg_delta_off), reinterpret_cast<float*>(ws + w.dq_acc_off),
-      /*zero_acc=*/true, static_cast<cudaStream_t>(stream));
+      reinterpret_cast<float*>(ws + w.neg_delta_off),
+      reinterpret_cast<fa::DqTileCount*>(ws + w.dq_cnt_off), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -455,8 +458,10 @@ fa_status fa_bwd_dq_convert(void* dQ, int B, int H, int N, int d, float scale, v
   const fa::Workspace w = fa::workspace_layout(BH, N, d);
   if ((st = check_workspace(workspace, workspace_bytes, w.total)) != FA_OK) return st;
   if ((st = check_device()) != FA_OK) return st;
+  char* ws = static_cast<char*>(workspace);
   cudaError_t e = fa::launch_bwd_dq_convert(
-      d, reinterpret_cast<const float*>(static_cast<char*>(workspace) + w.dq_acc_off), dQ, BH, N,
+      d, reinterpret_cast<const float*>(ws + w.dq_acc_off),
+      reinterpret_cast<const fa::DqTileCount*>(ws + w.dq_cnt_off), dQ, BH, N,
       resolve_scale(scale, d), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

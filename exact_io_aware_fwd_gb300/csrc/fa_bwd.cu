@@ -10,31 +10,40 @@
 // Kernels:
 //  bwd_preprocess  -D = -rowsum(dO o O) and -LSE * log2(e) into the workspace (negated so that
 //                  P and dP - D are single packed FMA / add instructions; padded rows get 0 and
-//                  -inf, which makes their recomputed P exactly 0), and zeroes the float32 dQ
-//                  accumulator.
+//                  -inf, which makes their recomputed P exactly 0), and resets the record of
+//                  every query tile of fa_bwd's dQ accumulation.
 //  bwd_dkdv        one CTA per (b, h, 128-key tile j); dK_j and dV_j accumulate in tensor memory
 //                  over the query tiles i (causal: i >= j only).  Warps: TMA producer, MMA
-//                  issuer, two idle, and kGroups warpgroups that each handle 128 / kGroups of
-//                  the 128 query columns of every key row for P and dS, drain their share of
-//                  dQ_{i-1} between P_i and dS_i (while dP_i runs), and write their share of the
-//                  dV and dK panels at the end.  Per query tile:
+//                  issuer, the dQ claim warp, one idle, and kGroups warpgroups that each handle
+//                  128 / kGroups of the 128 query columns of every key row for P and dS, drain
+//                  their share of dQ_{i-1} between P_i and dS_i (while dP_i runs), and write
+//                  their share of the dV and dK panels at the end.  Per query tile:
 //                    S^T = K_j Q_i^T and dP^T = V_j dO_i^T   (tcgen05, both operands in smem)
 //                    P^T = exp2(S^T * scale * log2 e - LSE_i * log2 e), written back over S^T
 //                    dS^T = P^T o (dP^T - D_i), written back over dP^T and to smem
 //                    dV += P^T dO_i, dK += dS^T Q_i          (A operand read from tensor memory)
 //                    dQ_i = dS K_j                            (A = dS from smem, MN-major)
-//                  and a warpgroup adds dQ_i into the float32 accumulator with vector
-//                  reductions (red.global.add.v4.f32).  Those atomics make the result
-//                  non-deterministic in the last bits, as the pages note for the default
-//                  backward (page "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section
-//                  "反向传播：用重计算代替存储").
-//  bwd_dq_convert  dQ = bf16(scale * accumulator).
+//  bwd_dq_convert  dQ = bf16(scale * accumulator), or 0 for a query tile nobody claimed.
+//
+// dQ across key tiles.  dQ_i = sum_j dS_ij K_j gets one partial per key tile j that visits query
+// tile i, from different CTAs in no fixed order.  The partials meet in a float32 accumulator in
+// the workspace, which is never zeroed:
+//   * the first key tile to claim the query tile (an atomic increment of the tile's record,
+//     made about a tile period before its partial is drained) stores its partial, in whole
+//     128-byte lines, so the accumulator's lines need no read from device memory;
+//   * every other one adds its partial with vector reductions (red.global.add.v4.f32) once the
+//     record shows that the first one's stores are visible.
+// The additions make dQ non-deterministic in the last bits, as the pages note for the default
+// backward (page "FlashAttention 入门：从 FA1 到 FA4 的 IO 感知注意力", section
+// "反向传播：用重计算代替存储"); dK and dV are accumulated in a fixed order.  Without a causal mask
+// key tile j visits the query tiles starting at tile j (j, j + 1, ..., wrapping around), so that
+// the claims of a query tile arrive a tile period apart, as they do under the causal order.
 //
 // dQ accumulator layout ("tile-major"): for (b, h), query tile i, column group g (4 floats)
 // and row r of the tile, element (r, 4g + e) is at float index
 //   (((bh * num_qtiles + i) * (d / 4) + g) * 128 + r) * 4 + e,
 // so that 32 consecutive rows of one column group are 512 contiguous bytes and a warp's
-// vector reduction is fully coalesced.
+// vector reduction (or store) covers four whole 128-byte lines.
 #include <type_traits>
 
 #include "fa_internal.h"
@@ -49,7 +58,8 @@ Workspace workspace_layout(int BH, int N, int d) {
   w.dq_acc_off = 0;
   w.neg_lse2_off = up(static_cast<size_t>(BH) * npad * d * sizeof(float));
   w.neg_delta_off = w.neg_lse2_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
-  w.total = w.neg_delta_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  w.dq_cnt_off = w.neg_delta_off + up(static_cast<size_t>(BH) * npad * sizeof(float));
+  w.total = w.dq_cnt_off + up(static_cast<size_t>(BH) * (npad / kTileRows) * sizeof(DqTileCount));
   return w;
 }
 
@@ -105,8 +115,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
                                                              const float* __restrict__ lse, int N,
                                                              int nqt, float* __restrict__ neg_lse2,
                                                              float* __restrict__ neg_delta,
-                                                             float* __restrict__ dq_acc,
-                                                             int zero_acc, int tph, RowGeo geo) {
+                                                             DqTileCount* __restrict__ recs,
+                                                             int tph, RowGeo geo) {
   constexpr int G = D / 8;     // lanes per row (8 bf16 = 16 bytes each)
   constexpr int RPW = 32 / G;  // rows per warp per pass
   const int i = static_cast<int>(blockIdx.x % tph);
@@ -139,17 +149,15 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const __nv_bfloat16
       neg_delta[idx] = (q < tr.n) ? -acc : 0.f;
     }
   }
-  if (!zero_acc) return;
-  float4* t = reinterpret_cast<float4*>(dq_acc + tr.ws_tile * 128 * D);
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int idx = threadIdx.x; idx < 32 * D; idx += 256) t[idx] = z;
+  if (recs != nullptr && threadIdx.x == 0) recs[tr.ws_tile].word = 0ull;  // nobody claimed it yet
 }
 
 // ------------------------------------------------------------------------------------------
 // dQ convert: the preprocess kernel's 1-D grid, 256 threads; thread = (row r, pair of column
-// groups).
+// groups).  A tile that no key tile claimed has no partial in the accumulator: its dQ is 0.
 template <int D, bool kVarlen>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ acc,
+                                                             const DqTileCount* __restrict__ recs,
                                                              __nv_bfloat16* __restrict__ dQ, int N,
                                                              int nqt, float scale, int tph,
                                                              RowGeo geo) {
@@ -159,6 +167,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   const int q = i * 128 + r;
   if (q >= tr.n) return;
   const float* tile = acc + tr.ws_tile * 128 * D;
+  // (the accumulator is read either way, so that its loads need not wait for the record's)
+  const bool claimed = static_cast<uint32_t>(__ldg(&recs[tr.ws_tile].word)) != 0u;
   // 16 columns of row r per step: four 16-byte loads (a warp reads 32 consecutive rows of one
   // 4-column group, 512 contiguous bytes each), then the whole 32-byte sector of bf16 output
   // written by this thread (two 16-byte stores back to back), so no output sector is assembled
@@ -167,8 +177,10 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __rest
   for (int ch = threadIdx.x >> 7; ch < D / 16; ch += 2) {
     float4 a[4];
 #pragma unroll
-    for (int g = 0; g < 4; ++g)
+    for (int g = 0; g < 4; ++g) {
       a[g] = __ldg(reinterpret_cast<const float4*>(tile + ((4 * ch + g) * 128 + r) * 4));
+      if (!claimed) a[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     uint32_t w[8];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
@@ -197,9 +209,11 @@ struct BwdLayout {
   static constexpr uint32_t kDelta = kLse + 1024;  // 2 stages x 128 floats
   static constexpr uint32_t kBar = kDelta + 1024;
   // kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, p_full, dp_full, ds_full,
-  // dq_full, dq_empty, dkdv_full, mma_done
-  static constexpr int kNumBars = 17;
-  static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
+  // dq_full, dq_empty, dkdv_full, mma_done, then the dQ claims' mode_full[2], mode_empty[2],
+  // first_stored[2]
+  static constexpr int kNumBars = 23;
+  static constexpr uint32_t kMode = kBar + kNumBars * 8;  // 2 slots: how a drain writes
+  static constexpr uint32_t kTmemSlot = kMode + 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4;
   // TMEM columns.  S^T (fp32) in [0, 128); P^T packed as bf16 pairs over the first half of each
@@ -228,6 +242,24 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
 }
 
 constexpr int kBwdThreads = 128 * (1 + kGroups);
+
+// How the drain warps write one partial dQ tile (see "dQ across key tiles" above).
+enum : int { kModeAdd = 0, kModeFirst = 1 };
+
+// Waits until the first claimant of a query tile has stored its partial (bit 63 of the tile's
+// word).  Bounded like every pipeline wait.
+__device__ __forceinline__ bool wait_first_stored(const uint64_t* word, const Ctl& c) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_u64(word) & kDqStored) return true;
+    if (*c.abort_flag) return false;
+    if (globaltimer_ns() - t0 > c.timeout_ns) {
+      ctl_fail(c, kErrTimeout);
+      return false;
+    }
+  }
+}
 
 // kWithDQ = false: the deterministic variant, dQ is computed by bwd_dq_kernel instead (no dQ
 // GEMM, no drain, no atomics, no dS copy in shared memory).
@@ -261,6 +293,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* dq_empty = bars + 14;
   uint64_t* dkdv_full = bars + 15;
   uint64_t* mma_done = bars + 16;
+  uint64_t* mode_full = bars + 17;     // [2] the claim warp published how a drain writes
+  uint64_t* mode_empty = bars + 19;    // [2] every drain warp took it (its drain has begun)
+  uint64_t* first_stored = bars + 21;  // [2] every drain warp issued its stores of a first partial
+  volatile int* mode_slot = reinterpret_cast<volatile int*>(sm + L::kMode);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const Ctl ctl{abort_flag, a.status, a.timeout_ns};
@@ -304,19 +340,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     c_list = base + BI.cidx + static_cast<int64_t>(j) * nqt;
     nI = (j * 128 < kv_len) ? __ldg(base + (a.causal ? BI.cccnt : BI.ccnt) + j) : 0;
   }
-  auto qtile = [&](int it) { return kSparse ? __ldg(c_list + it) : i0 + it; };
+  // without a causal mask key tile j starts at query tile j and wraps around, so the key tiles of
+  // a head reach any one query tile a tile period apart (dQ accumulation, see above)
+  auto qtile = [&](int it) {
+    if constexpr (kSparse) return __ldg(c_list + it);
+    return a.causal ? i0 + it : (j + it < nqt ? j + it : j + it - nqt);
+  };
   // iteration it -> (query head of the group, query tile); G == 1 without grouped queries
   auto head_of = [&](int it) { return hk * G + (G == 1 ? 0 : it / nI); };
   auto tile_of = [&](int it) { return qtile(G == 1 ? it : it % nI); };
   const int nIt = nI * G;  // iterations of the CTA
+  // workspace tile (record, accumulator tile) of query head qh, query tile qt
+  auto ws_tile_of = [&](int qh, int qt) {
+    return static_cast<size_t>(ws_head(qh)) * a.ws_tiles + ws_tile0 + qt;
+  };
 
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
     for (int k = 0; k < L::kNumBars; ++k) {
-      // P, dS and the release of dQ_i's tensor memory are signalled by every warp of the
-      // elementwise warpgroups
+      // P, dS, the release of dQ_i's tensor memory and the drain barriers are signalled by every
+      // warp of the elementwise warpgroups
       uint32_t count = 1;
-      if (&bars[k] == p_full || &bars[k] == ds_full || &bars[k] == dq_empty) count = 4 * kGroups;
+      if (&bars[k] == p_full || &bars[k] == ds_full || &bars[k] == dq_empty ||
+          &bars[k] == &mode_empty[0] || &bars[k] == &mode_empty[1] ||
+          &bars[k] == &first_stored[0] || &bars[k] == &first_stored[1])
+        count = 4 * kGroups;
       mbar_init(&bars[k], count);
     }
     fence_mbar_init();
@@ -473,6 +521,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mma_commit(mma_done);
       drain_wait(mma_done, 0, ctl);
     }
+  } else if (warp == 2 || warp == 3) {
+    // ================= dQ claims (one thread of each warp; warp 2 the even iterations, warp 3
+    // the odd ones).  Claims each query tile and tells the drain warps whether to store its
+    // partial (the tile's first claimant) or add it (any later one, once the first one's stores
+    // are visible).  A claim is an acquiring atomic add on the tile's word, whose old value also
+    // says whether the first partial is stored yet.  An atomic from this SM waits behind the SM's
+    // own dQ additions in flight (thousands of cycles, about a tile period) and an acquiring one
+    // holds back its thread's later memory operations meanwhile, so each thread serves every
+    // other iteration and claims two drains ahead: iteration it at the start of the drain of it - 2
+    // (iteration 0 at the start, iteration 1 at the drain of 0).  Claims thus follow the order of
+    // the drains, and under the causal order (and the rotated non-causal one) the first claimant of
+    // a tile is the key tile that drains it first.  After the drain warps have issued a first
+    // partial's stores, a fence orders them before the record's bit 63.
+    if (kWithDQ && lane == 0 && nIt > warp - 2) {
+      const int par = static_cast<int>(warp) - 2;  // the iterations it with it % 2 == par
+      auto rec = [&](int it) { return &a.dq_cnt[ws_tile_of(head_of(it), tile_of(it))].word; };
+      int firsts = 0;  // first partials among this thread's iterations (phases of first_stored)
+      int prev_first = -1;  // the previous iteration of this thread, if it stored a first partial
+      bool ok = true;
+      for (int it = par; ok && it < nIt; it += 2) {
+        // claim time: the start of the drain of it - 2 (of 0 for iteration 1)
+        if (it >= 1 && !(ok = mbar_wait(&mode_empty[it < 2 ? 0 : it & 1],
+                                        it < 2 ? 0u : ((it - 2) >> 1) & 1, ctl)))
+          break;
+        if (prev_first >= 0) {  // the drain of prev_first has begun: its stores are next
+          if (!(ok = mbar_wait(&first_stored[par], firsts & 1, ctl))) break;
+          ++firsts;
+          fence_acq_rel_gpu();  // the drain warps' stores (seen through first_stored) go first
+          red_add_relaxed_u64(rec(prev_first), kDqStored);
+          prev_first = -1;
+        }
+        const uint64_t old = atom_add_acquire_u64(rec(it), 1ull);
+        const bool first = static_cast<uint32_t>(old) == 0u;
+        if (!first && !(old & kDqStored) && !(ok = wait_first_stored(rec(it), ctl))) break;
+        mode_slot[it & 1] = first ? kModeFirst : kModeAdd;
+        mbar_arrive(&mode_full[it & 1]);
+        if (first) prev_first = it;
+      }
+      if (ok && prev_first >= 0) {  // the last iteration of this thread stored a first partial
+        if (mbar_wait(&first_stored[par], firsts & 1, ctl)) {
+          fence_acq_rel_gpu();
+          red_add_relaxed_u64(rec(prev_first), kDqStored);
+        }
+      }
+    }
   } else if (warp >= 4) {
     // ================= P, dS, the dQ drain and the epilogue: one thread per row of the tile,
     // one warpgroup per kQG query columns of P / dS and D / kGroups columns of dQ
@@ -510,10 +603,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     uint32_t dq_late[4 * (kLate > 0 ? kLate : 1)];
     float* late_tile = nullptr;
     auto drain = [&](int it, int qh, int qt) -> bool {  // (qh, qt): query head, tile of it
+      if (!mbar_wait_warp(&mode_full[it & 1], (it >> 1) & 1, ctl)) return false;
+      const int mode = mode_slot[it & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mode_empty[it & 1]);
       if (!mbar_wait_warp(dq_full, it & 1, ctl)) return false;
       tc_fence_after();
-      float* tile =
-          a.dq_acc + (static_cast<size_t>(ws_head(qh)) * a.ws_tiles + ws_tile0 + qt) * 128 * D;
+      float* tile = a.dq_acc + ws_tile_of(qh, qt) * 128 * D;
       const int g0 = kGroups4 * grp;  // first 4-column group of this group's columns
       uint32_t v[kDC];
       if constexpr (kDC == 64) {
@@ -529,6 +625,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
+      if (mode == kModeFirst) {  // the tile's first partial: stored, whole lines per warp
+#pragma unroll
+        for (int g = 0; g < kGroups4; ++g)
+          st_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
+                __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                __uint_as_float(v[4 * g + 3]));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&first_stored[it & 1]);
+        return true;
+      }
 #pragma unroll
       for (int g = 0; g < kGroups4 - kLate; ++g)
         red_add_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
@@ -539,7 +645,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       late_tile = tile + (g0 + kGroups4 - kLate) * 128 * 4;
       return true;
     };
-    auto drain_late = [&]() {  // the deferred atomics of the last drain, if any
+    auto drain_late = [&]() {  // the deferred additions of the last drain, if any
       if (late_tile == nullptr) return;
 #pragma unroll
       for (int g = 0; g < kLate; ++g)
@@ -732,8 +838,8 @@ unsigned flat_grid(long long tiles, long long heads) {
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse, int BH,
-                                  int N, float* neg_lse2, float* neg_delta, float* dq_acc,
-                                  bool zero_acc, cudaStream_t s) {
+                                  int N, float* neg_lse2, float* neg_delta, DqTileCount* recs,
+                                  cudaStream_t s) {
   const int nqt = (N + 127) / 128;
   const unsigned grid = flat_grid(nqt, BH);
   if (grid == 0) return cudaErrorInvalidConfiguration;
@@ -742,19 +848,17 @@ cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const fl
   const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
     bwd_preprocess_kernel<64, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2, neg_delta,
-                                                           dq_acc, zero_acc ? 1 : 0, nqt, geo);
+                                                           recs, nqt, geo);
   else
     bwd_preprocess_kernel<128, false><<<grid, 256, 0, s>>>(o, g, lse, N, nqt, neg_lse2,
-                                                            neg_delta, dq_acc, zero_acc ? 1 : 0,
-                                                            nqt, geo);
+                                                            neg_delta, recs, nqt, geo);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, const float* lse,
                                          const int32_t* cu, int B, int H, int max_tiles,
                                          int total, int ws_tiles, float* neg_lse2,
-                                         float* neg_delta, float* dq_acc, bool zero_acc,
-                                         cudaStream_t s) {
+                                         float* neg_delta, DqTileCount* recs, cudaStream_t s) {
   const unsigned grid = flat_grid(max_tiles, static_cast<long long>(B) * H);
   if (grid == 0) return cudaErrorInvalidConfiguration;
   auto o = static_cast<const __nv_bfloat16*>(O);
@@ -762,40 +866,43 @@ cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, c
   const RowGeo geo{cu, H, total, ws_tiles};
   if (d == 64)
     bwd_preprocess_kernel<64, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
-                                                          dq_acc, zero_acc ? 1 : 0, max_tiles, geo);
+                                                          recs, max_tiles, geo);
   else
     bwd_preprocess_kernel<128, true><<<grid, 256, 0, s>>>(o, g, lse, 0, 0, neg_lse2, neg_delta,
-                                                           dq_acc, zero_acc ? 1 : 0, max_tiles,
-                                                           geo);
+                                                           recs, max_tiles, geo);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N, float scale,
-                                  cudaStream_t s) {
+cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, const DqTileCount* recs, void* dQ,
+                                  int BH, int N, float scale, cudaStream_t s) {
   const int nqt = (N + 127) / 128;
   const unsigned grid = flat_grid(nqt, BH);
   if (grid == 0) return cudaErrorInvalidConfiguration;
   auto out = static_cast<__nv_bfloat16*>(dQ);
   const RowGeo geo{nullptr, 1, 0, 0};
   if (d == 64)
-    bwd_dq_convert_kernel<64, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, nqt, geo);
+    bwd_dq_convert_kernel<64, false><<<grid, 256, 0, s>>>(dq_acc, recs, out, N, nqt, scale, nqt,
+                                                           geo);
   else
-    bwd_dq_convert_kernel<128, false><<<grid, 256, 0, s>>>(dq_acc, out, N, nqt, scale, nqt, geo);
+    bwd_dq_convert_kernel<128, false><<<grid, 256, 0, s>>>(dq_acc, recs, out, N, nqt, scale, nqt,
+                                                            geo);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, void* dQ, const int32_t* cu,
-                                         int B, int H, int max_tiles, int total, int ws_tiles,
-                                         float scale, cudaStream_t s) {
+cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, const DqTileCount* recs,
+                                         void* dQ, const int32_t* cu, int B, int H,
+                                         int max_tiles, int total, int ws_tiles, float scale,
+                                         cudaStream_t s) {
   const unsigned grid = flat_grid(max_tiles, static_cast<long long>(B) * H);
   if (grid == 0) return cudaErrorInvalidConfiguration;
   auto out = static_cast<__nv_bfloat16*>(dQ);
   const RowGeo geo{cu, H, total, ws_tiles};
   if (d == 64)
-    bwd_dq_convert_kernel<64, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, max_tiles, geo);
+    bwd_dq_convert_kernel<64, true><<<grid, 256, 0, s>>>(dq_acc, recs, out, 0, 0, scale, max_tiles,
+                                                          geo);
   else
-    bwd_dq_convert_kernel<128, true><<<grid, 256, 0, s>>>(dq_acc, out, 0, 0, scale, max_tiles,
-                                                           geo);
+    bwd_dq_convert_kernel<128, true><<<grid, 256, 0, s>>>(dq_acc, recs, out, 0, 0, scale,
+                                                           max_tiles, geo);
   return cudaGetLastError();
 }
 

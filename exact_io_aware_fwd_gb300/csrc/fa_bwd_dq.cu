@@ -47,19 +47,6 @@ struct DqLayout {
 };
 
 
-// Entries of the ascending list[0, cnt) below lim (whole warp).
-__device__ __forceinline__ int warp_count_below_dq(const int32_t* list, int cnt, int lim) {
-  int total = 0;
-  for (int c = 0; c < cnt; c += 32) {
-    const int idx = c + static_cast<int>(lane_id());
-    const bool ok = idx < cnt && __ldg(list + idx) < lim;
-    const unsigned m = __ballot_sync(0xffffffffu, ok);
-    total += __popc(m);
-    if (m != 0xffffffffu) break;
-  }
-  return total;
-}
-
 template <int D, bool kSparse, bool kVarlen>
 __global__ void __launch_bounds__(384, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -125,7 +112,7 @@ __global__ void __launch_bounds__(384, 1)
     const int32_t* base = a.blk + (a.blk_heads == 1 ? 0 : static_cast<int64_t>(bh % a.H) * BI.words);
     r_list = base + BI.ridx + static_cast<int64_t>(i) * nqt;
     if (warp == 2) {
-      const int c = warp_count_below_dq(r_list, __ldg(base + BI.rcnt + i), nb_dense);
+      const int c = warp_count_below(r_list, __ldg(base + BI.rcnt + i), nb_dense);
       if (lane == 0) *cnt_smem = c;
     }
   }

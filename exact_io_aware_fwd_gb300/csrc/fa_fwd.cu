@@ -131,20 +131,6 @@ struct FwdLayout {
   static constexpr uint32_t kTmemCols = kHalf ? 256 : 512;
 };
 
-// Number of entries of the ascending list[0, cnt) below lim (whole warp; a sorted list fails the
-// test only after its last passing entry).
-__device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, int lim) {
-  int total = 0;
-  for (int c = 0; c < cnt; c += 32) {
-    const int idx = c + static_cast<int>(lane_id());
-    const bool ok = idx < cnt && __ldg(list + idx) < lim;
-    const unsigned m = __ballot_sync(0xffffffffu, ok);
-    total += __popc(m);
-    if (m != 0xffffffffu) break;
-  }
-  return total;
-}
-
 template <int D, bool kSparse, bool kVarlen>
 __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
                                   (kHalfSteps<D, kSparse, kVarlen> ? 2 : 1))

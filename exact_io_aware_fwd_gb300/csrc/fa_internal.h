@@ -72,6 +72,19 @@ struct FwdArgs {
   uint32_t smem_bytes;    // dynamic shared memory actually granted
 };
 
+// Record of one 128-row query tile of one head in fa_bwd's dQ accumulation (16 bytes, in the
+// workspace; reset by the preprocess).  The key tiles that contribute a partial dQ to the tile
+// coordinate through one 64-bit word: each adds 1 to it to claim the tile (the low 32 bits count
+// the claims), and the first claimant, once its partial is stored into the accumulator, sets bit
+// 63, after which the others add theirs.  One atomic thus tells a claimant both whether it is
+// the first and whether the first one's stores are visible.  A tile nobody claimed (no key tile
+// contributes) is converted as zeros.
+struct DqTileCount {
+  uint64_t word;
+  uint64_t spare;
+};
+constexpr uint64_t kDqStored = 1ull << 63;  // the first claimant's partial is in the accumulator
+
 struct BwdArgs {
   int H, N, BH;
   int Hkv;                // key/value heads (grouped-query attention when < H)
@@ -90,6 +103,7 @@ struct BwdArgs {
   const float* neg_lse2;  // workspace: -LSE * log2(e), [BH][Npad], -inf on padded rows
   const float* neg_delta; // workspace: -D = -rowsum(dO o O), [BH][Npad], 0 on padded rows
   float* dq_acc;          // workspace: dQ accumulator, tile-major (see fa_bwd.cu)
+  DqTileCount* dq_cnt;    // workspace: per query tile records of the dQ accumulation
   const int32_t* blk;     // block-sparse index or nullptr (as in FwdArgs)
   int blk_heads;
   int* status;
@@ -97,10 +111,11 @@ struct BwdArgs {
   uint32_t smem_bytes;
 };
 
-// Workspace layout (all offsets 256-byte aligned): dq_acc | -LSE*log2(e) | -D.  BH heads of N
-// rows padded to 128; the variable-length workspace is workspace_layout(H, ws_tiles * 128, d).
+// Workspace layout (all offsets 256-byte aligned): dq_acc | -LSE*log2(e) | -D | tile records.
+// BH heads of N rows padded to 128; the variable-length workspace is
+// workspace_layout(H, ws_tiles * 128, d).
 struct Workspace {
-  size_t dq_acc_off, neg_lse2_off, neg_delta_off, total;
+  size_t dq_acc_off, neg_lse2_off, neg_delta_off, dq_cnt_off, total;
 };
 Workspace workspace_layout(int BH, int N, int d);
 
@@ -122,19 +137,20 @@ cudaError_t ensure_smem_limit(uint32_t bytes) {
 // Launchers return cudaSuccess or the launch error.
 cudaError_t launch_fwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t s);
+// recs: reset the tile records of fa_bwd's dQ accumulation, or nullptr (deterministic path)
 cudaError_t launch_bwd_preprocess(int d, const void* O, const void* dO, const float* lse,
-                                  int BH, int N, float* neg_lse2, float* neg_delta, float* dq_acc,
-                                  bool zero_acc, cudaStream_t s);
+                                  int BH, int N, float* neg_lse2, float* neg_delta,
+                                  DqTileCount* recs, cudaStream_t s);
 // variable-length preprocess / dQ conversion: grid over (tile, b, h) of a packed batch
 cudaError_t launch_bwd_preprocess_varlen(int d, const void* O, const void* dO, const float* lse,
                                          const int32_t* cu, int B, int H, int max_tiles,
                                          int total, int ws_tiles, float* neg_lse2,
-                                         float* neg_delta, float* dq_acc, bool zero_acc,
+                                         float* neg_delta, DqTileCount* recs, cudaStream_t s);
+cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, const DqTileCount* recs,
+                                         void* dQ, const int32_t* cu, int B, int H,
+                                         int max_tiles, int total, int ws_tiles, float scale,
                                          cudaStream_t s);
-cudaError_t launch_bwd_dq_convert_varlen(int d, const float* dq_acc, void* dQ, const int32_t* cu,
-                                         int B, int H, int max_tiles, int total, int ws_tiles,
-                                         float scale, cudaStream_t s);
-// with_dq: accumulate dQ with atomics (fa_bwd); without: dK, dV only (deterministic path)
+// with_dq: also accumulate dQ in the workspace (fa_bwd); without: dK, dV only (deterministic path)
 cudaError_t launch_bwd_dkdv(int d, bool with_dq, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo,
                             const CUtensorMap& tdk, const CUtensorMap& tdv, const BwdArgs& a,
@@ -146,7 +162,7 @@ cudaError_t launch_bwd_dq(int d, const CUtensorMap& tq, const CUtensorMap& tk,
 // block-sparse index of mask_heads masks [T][T] into `index` (mask_heads * words int32)
 cudaError_t launch_block_index(const uint8_t* mask, int T, int mask_heads, int32_t* index,
                                cudaStream_t s);
-cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, void* dQ, int BH, int N,
-                                  float scale, cudaStream_t s);
+cudaError_t launch_bwd_dq_convert(int d, const float* dq_acc, const DqTileCount* recs, void* dQ,
+                                  int BH, int N, float scale, cudaStream_t s);
 
 }  // namespace fa

@@ -441,6 +441,45 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// Number of entries of the ascending list[0, cnt) below lim (whole warp; a sorted list fails the
+// test only after its last passing entry).
+__device__ __forceinline__ int warp_count_below(const int32_t* list, int cnt, int lim) {
+  int total = 0;
+  for (int c = 0; c < cnt; c += 32) {
+    const int idx = c + static_cast<int>(lane_id());
+    const bool ok = idx < cnt && __ldg(list + idx) < lim;
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    total += __popc(m);
+    if (m != 0xffffffffu) break;
+  }
+  return total;
+}
+
+// ------------------------------------------------------------------------------------------
+// Global-memory synchronisation between CTAs (the dQ accumulation protocol of the dK/dV kernel)
+__device__ __forceinline__ uint64_t atom_add_acquire_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.acquire.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void red_add_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Orders this thread's earlier memory operations, and those of other threads that it has
+// synchronised with (cumulativity), before its later ones, at GPU scope.
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+__device__ __forceinline__ void st_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gaddr), "f"(a), "f"(b),
                "f"(c), "f"(d)

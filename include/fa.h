@@ -62,9 +62,9 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
                  const int32_t* kv_lens, void* stream);
 
 /*
- * Bytes of workspace fa_bwd needs for these sizes: a float32 dQ accumulator plus the per-row
+ * Bytes of workspace fa_bwd needs for these sizes: a float32 dQ accumulator, the per-row
  * statistics -D = -rowsum(dO o O) and -LSE * log2(e), each padded to a multiple of 128 rows per
- * (b, h).  Returns 0 for invalid sizes.
+ * (b, h), and a 16-byte record per 128-row query tile.  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
@@ -86,12 +86,16 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 /*
  * The three stages of fa_bwd, exported so that each can be launched (and timed) on its own.
  * They must run in this order on one stream with the same arguments and workspace.
- *  fa_bwd_preprocess: -D_i = -sum_k dO_ik O_ik, -LSE_i * log2(e) into the workspace, zeroes
- *                     the dQ accumulator (first page, 关键设计三, D_i = dO_i^T O_i).
+ *  fa_bwd_preprocess: -D_i = -sum_k dO_ik O_ik, -LSE_i * log2(e) into the workspace, and
+ *                     resets every query tile's record (first page, 关键设计三,
+ *                     D_i = dO_i^T O_i).  The dQ accumulator itself is not touched.
  *  fa_bwd_dkdv:       one pass over the query tiles per key tile: recomputes P^T from LSE,
- *                     writes dK, dV and adds dS K into the dQ accumulator with float32
- *                     atomics (non-deterministic in the last bits).
- *  fa_bwd_dq_convert: dQ = bf16(scale * accumulator).
+ *                     writes dK, dV, and puts each key tile's partial dS K into the dQ
+ *                     accumulator: the first key tile to claim a query tile (through its record)
+ *                     stores its partial, the others add theirs with float32 atomics once it has
+ *                     (non-deterministic in the last bits).
+ *  fa_bwd_dq_convert: dQ = bf16(scale * accumulator); 0 for a query tile that no key tile
+ *                     claimed (every key masked).
  */
 fa_status fa_bwd_preprocess(const void* O, const void* dO, const float* LSE,
                             int B, int H, int N, int d,
@@ -212,8 +216,9 @@ fa_status fa_bwd_block_sparse(const void* Q, const void* K, const void* V, const
  * B * H * roundup(N, 128); at d = 64 about 254,000).  Nothing is allocated.  The first call on
  * each device looks up the array's device address with that device current; make it before
  * any stream capture.  All calls share the array: calls that overlap on the GPU race and must
- * be serialised by the caller.  Every part of the array a call reads is first rewritten by the
- * same call (the dQ accumulator is zeroed), so earlier contents never affect a result.
+ * be serialised by the caller.  Every part of the array a call reads is first written by the
+ * same call (the statistics and tile records by its first stage, each accumulator tile by the
+ * first key tile that contributes to it), so earlier contents never affect a result.
  */
 fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
                          const void* dO, const float* LSE, void* dQ, void* dK, void* dV,

@@ -779,3 +779,161 @@ def dq_kernel(nb, seed, bug=None, abort_at=None, conditional_drain=False):
         assert acc["dQ"] == nb
         assert sim.exit_copies == 0 and sim.exit_ops == 0, (sim.exit_copies, sim.exit_ops)
     return sim
+
+
+# ------------------------------------------------------------------------------------------
+# dQ accumulation across the dK/dV kernel's CTAs (bwd_dkdv_kernel's claim threads and drains):
+# every key tile (CTA) that visits a query tile claims it with an atomic add on the tile's word;
+# the first claimant stores its partial, the others add theirs once the word's "stored" bit is
+# set, which the first one's claim thread sets after a fence that waits for its stores to be
+# visible.  Two claim threads per CTA (even / odd iterations) claim two drains ahead and publish
+# each drain's mode through mode_full / mode_empty; the drain warps signal first_stored.  Stores
+# and additions reach memory after random delays (memory visibility); a bounded number of CTAs is
+# resident at a time, launched in key-tile order (a CTA waiting on a tile's first claimant must
+# never wait for a CTA that cannot start).
+
+def dq_claims(nkt, causal, seed, resident=3, W=2, bug=None, abort_at=None):
+    """nkt key tiles (CTAs) of one head over nkt query tiles.  `bug` plants a protocol error:
+    "no_wait": a later claimant adds without waiting for the stored bit; "no_fence": the first
+    claimant sets the stored bit without waiting for its stores to be visible.  "claim_at_start"
+    makes every claim when the CTA starts (claims then no longer follow the drains: correct, but
+    later claimants wait longer).  Returns the Sim; asserts that every query tile ends with each
+    of its contributions exactly once."""
+    sim = Sim(seed, abort_at)
+    wait_ok = sim.wait_ok
+    rng = sim.rng
+    word = [{"claims": 0, "stored": False} for _ in range(nkt)]
+    acc = [None for _ in range(nkt)]       # set of contributions in memory (None: uninitialised)
+    pending_stores = {j: 0 for j in range(nkt)}  # stores of CTA j not yet visible
+
+    def tiles_of(j):
+        return list(range(j, nkt)) if causal else [(j + k) % nkt for k in range(nkt)]
+
+    def memory_op(fn):  # takes effect after a random delay
+        sim.copy(fn)
+
+    def cta(j):
+        tiles = tiles_of(j)
+        n = len(tiles)
+        mode_full = [Bar(1, f"mode_full{j},{s}") for s in range(2)]
+        mode_empty = [Bar(W, f"mode_empty{j},{s}") for s in range(2)]
+        first_stored = [Bar(W, f"first_stored{j},{s}") for s in range(2)]
+        slot = [None, None]
+        done = {"left": 0}
+
+        def claim(it):
+            t = tiles[it]
+            old = dict(word[t])
+            word[t]["claims"] += 1
+            return old
+
+        early = {}
+        if bug == "claim_at_start":
+            for it in range(n):
+                early[it] = claim(it)
+
+        def claimer(par):
+            firsts, prev_first = 0, None
+            for it in range(par, n, 2):
+                if it >= 1:
+                    bar, ph = (mode_empty[0], 0) if it < 2 else (mode_empty[it & 1], ((it - 2) >> 1) & 1)
+                    if not (yield from wait_ok(bar, ph, (it - 2) // 2 + 1 if it >= 2 else 1)):
+                        return
+                if prev_first is not None:
+                    if not (yield from wait_ok(first_stored[par], firsts & 1, firsts + 1)):
+                        return
+                    firsts += 1
+                    if bug != "no_fence":
+                        while pending_stores[j]:  # the fence: this CTA's stores are visible
+                            yield
+                    t_prev = tiles[prev_first]
+
+                    def set_stored(t=t_prev):
+                        word[t]["stored"] = True
+                    memory_op(set_stored)
+                    prev_first = None
+                old = early[it] if bug == "claim_at_start" else claim(it)
+                yield
+                first = old["claims"] == 0
+                if not first and not old["stored"] and bug != "no_wait":
+                    while not word[tiles[it]]["stored"]:  # wait_first_stored
+                        if sim.abort:
+                            return
+                        sim.spins += 1
+                        if sim.abort_at is not None and sim.spins == sim.abort_at:
+                            sim.abort = True
+                            return
+                        yield
+                slot[it & 1] = "first" if first else "add"
+                mode_full[it & 1].arrive()
+                if first:
+                    prev_first = it
+            if prev_first is not None:
+                if (yield from wait_ok(first_stored[par], firsts & 1, firsts + 1)):
+                    while pending_stores[j]:
+                        yield
+
+                    def set_stored_last(t=tiles[prev_first]):
+                        word[t]["stored"] = True
+                    memory_op(set_stored_last)
+
+        def drain_warp(w):
+            for it in range(n):
+                if not (yield from wait_ok(mode_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)):
+                    return
+                mode = slot[it & 1]
+                mode_empty[it & 1].arrive()
+                yield
+                t = tiles[it]
+                contribution = (j, w)
+                if mode == "first":
+                    pending_stores[j] += 1
+
+                    def store(t=t, c=contribution):
+                        # a store reaching memory after an addition would erase that addition
+                        assert acc[t] is None or acc[t] <= {(j, x) for x in range(W)}, \
+                            f"tile {t}: the first partial lands after an addition {acc[t]}"
+                        acc[t] = (acc[t] or set()) | {c}
+                        pending_stores[j] -= 1
+                    memory_op(store)
+                    first_stored[it & 1].arrive()
+                else:
+                    def red(t=t, c=contribution):
+                        assert acc[t] is not None, f"tile {t}: addition into an uninitialised accumulator"
+                        acc[t] = acc[t] | {c}
+                    memory_op(red)
+
+        agents = [claimer(0), claimer(1)] + [drain_warp(w) for w in range(W)]
+        return agents
+
+    # the block scheduler: CTAs start in key-tile order, at most `resident` at a time
+    live_ctas = {"n": 0}
+
+    def launcher():
+        for j in range(nkt):
+            while live_ctas["n"] >= resident:
+                yield
+            live_ctas["n"] += 1
+            agents = cta(j)
+            left = {"n": len(agents)}
+
+            def wrap(a, left=left):
+                yield from a
+                left["n"] -= 1
+                if left["n"] == 0:
+                    live_ctas["n"] -= 1
+            for a in agents:
+                sim.spawn(wrap(a))
+            yield
+
+    def idle():  # the MMA-issuer slot of Sim.run: nothing is issued here
+        return
+        yield
+
+    sim.run([launcher()], idle())
+    if not sim.abort:
+        for t in range(nkt):
+            contributors = {j for j in range(nkt) if t in tiles_of(j)}
+            want = {(j, w) for j in contributors for w in range(W)}
+            assert acc[t] == want, (t, acc[t], want)
+    return sim

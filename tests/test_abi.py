@@ -42,11 +42,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # dq accumulator (N padded to 128 rows) + two padded per-row float arrays, 256-byte aligned
-    assert fa.fa_bwd_workspace_size(1, 1, 128, 64) == 128 * 64 * 4 + 2 * 512
+    # dq accumulator (N padded to 128 rows) + two padded per-row float arrays + a 16-byte record
+    # per 128-row tile, each part 256-byte aligned
+    up = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert fa.fa_bwd_workspace_size(1, 1, 128, 64) == 128 * 64 * 4 + 2 * 512 + 256
     n = fa.fa_bwd_workspace_size(2, 3, 2000, 128)
     npad = 2048
-    assert n == 6 * npad * 128 * 4 + 2 * ((6 * npad * 4 + 255) // 256 * 256)
+    assert n == 6 * npad * 128 * 4 + 2 * up(6 * npad * 4) + up(6 * (npad // 128) * 16)
     assert fa.fa_bwd_workspace_size(1, 1, 128, 96) == 0
     assert fa.fa_bwd_workspace_size(0, 1, 128, 64) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 0, 64) == 0
@@ -71,6 +73,7 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert lib.fa_bwd(*args, null, 1 << 20, null) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd(*args, p, 16, null) == fa.FA_ERR_WORKSPACE
     assert lib.fa_bwd_dq_convert(p, 1, 1, 8, 64, -1.0, null, 0, null) == fa.FA_ERR_WORKSPACE
+    assert lib.fa_bwd_preprocess(p, p, p, 1, 1, 8, 64, null, 0, null) == fa.FA_ERR_WORKSPACE
     # fa_bwd checks every 16-byte operand pointer (Q, K, V, O, dO, dQ, dK, dV; LSE needs only
     # 4 bytes) before its first launch, and before looking for a device
     for bad in (0, 1, 2, 3, 4, 6, 7, 8):

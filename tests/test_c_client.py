@@ -28,6 +28,6 @@ def test_c99_client_links_and_runs(tmp_path):
                          timeout=60).stdout.splitlines()
     got = dict(line.split(" ", 1) for line in out)
     assert got["status_string"] == "device pipeline wait timed out"
-    assert int(got["workspace"]) == 128 * 64 * 4 + 2 * 512
+    assert int(got["workspace"]) == 128 * 64 * 4 + 2 * 512 + 256  # + one 16-byte tile record
     assert int(got["unsupported"]) == fa.FA_ERR_UNSUPPORTED
     assert int(got["invalid"]) == fa.FA_ERR_INVALID_ARG

@@ -1,13 +1,14 @@
 """CPU model check of the kernels' mbarrier pipelines (tests/protocol_model.py): the forward
 (128-key steps, block-sparse streams with gaps, the d = 64 half steps), the dK/dV kernel and the deterministic dQ kernel run their roles' waits, arrivals
-and buffer reads and writes under many random interleavings, for every per-tile step count up to
+and buffer reads and writes under many random interleavings (and the dK/dV kernel's CTAs their
+claims on the shared dQ accumulator), for every per-tile step count up to
 a few stages past the ring's length; no deadlock, no wait on a wrong phase, no read of a stage
 before its copy or after its release.  Planted protocol errors (among them the dO race once found in
 the dK/dV kernel) must fail."""
 
 import pytest
 
-from protocol_model import dkdv, dq_kernel, forward
+from protocol_model import dkdv, dq_claims, dq_kernel, forward
 
 
 def _tile_steps(nmax):
@@ -147,3 +148,41 @@ def test_deterministic_dq_timeout_every_role_leaves():
     """The same for the deterministic dQ kernel."""
     for sim in _dq_abort_runs():
         assert sim.abort and sim.exit_ops == 0 and sim.exit_copies == 0
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_dq_claims_across_ctas(causal):
+    """The dK/dV kernel's CTAs sharing the dQ accumulator: whatever the interleaving, the memory
+    delays and the number of CTAs resident at a time (down to one: no CTA may wait for one that
+    cannot start), every query tile ends with each contribution exactly once, the first partial
+    stored before any addition reaches it."""
+    for nkt in (1, 2, 3, 5, 8):
+        for resident in (1, 2, 3, 8):
+            for seed in range(8):
+                dq_claims(nkt, causal, seed, resident=resident)
+
+
+def test_dq_claims_in_any_claim_order():
+    """Claims made out of the drains' order (all at a CTA's start) only make later claimants wait
+    longer; the result is the same."""
+    for causal in (True, False):
+        for seed in range(20):
+            dq_claims(6, causal, seed, resident=3, bug="claim_at_start")
+
+
+@pytest.mark.parametrize("bug", ["no_wait", "no_fence"])
+def test_checker_catches_dq_claim_errors(bug):
+    assert _fails(lambda seed: dq_claims(5, True, seed, resident=5, bug=bug))
+    assert _fails(lambda seed: dq_claims(5, False, seed, resident=5, bug=bug))
+
+
+def test_dq_claims_timeout_every_role_leaves():
+    """A wait (of any CTA) that runs past its limit: every role of every CTA leaves."""
+    import random
+
+    rng = random.Random(19)
+    for causal in (True, False):
+        for seed in range(6):
+            spins = dq_claims(5, causal, seed, resident=3).spins
+            for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(6, spins))):
+                assert dq_claims(5, causal, seed, resident=3, abort_at=abort_at).abort
