@@ -391,9 +391,12 @@ def cpu_cores():
 
 def host_link_gbs(h_in, h_out, stream, reps=3):
     """Plain copy rates of the host link just before the end-to-end run: `h_in` (pinned) to a
-    device buffer and back into `h_out` (pinned, same size), one direction at a time.  A slow
-    end-to-end figure with normal rates here is the pipeline's; with low rates, the link's."""
+    device buffer and back into `h_out` (pinned, same size), one direction at a time, then both
+    at once on two streams ("both": bytes of both directions per second).  A slow end-to-end
+    figure with normal rates here is the pipeline's; with low rates, the link's."""
     dbuf = torch.empty(h_in.shape, dtype=h_in.dtype, device=stream.device)
+    dbuf2 = torch.empty(h_in.shape, dtype=h_in.dtype, device=stream.device)
+    nbytes = h_in.numel() * h_in.element_size()
     rates = {}
     for name, copy in (("h2d", lambda: dbuf.copy_(h_in, non_blocking=True)),
                        ("d2h", lambda: h_out.copy_(dbuf, non_blocking=True))):
@@ -404,8 +407,20 @@ def host_link_gbs(h_in, h_out, stream, reps=3):
             copy()
         b.record(stream)
         b.synchronize()
-        rates[name] = reps * h_in.numel() * h_in.element_size() / (a.elapsed_time(b) * 1e6)
-    del dbuf
+        rates[name] = reps * nbytes / (a.elapsed_time(b) * 1e6)
+    other = torch.cuda.Stream(stream.device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    other.wait_stream(stream)
+    for _ in range(reps):
+        dbuf2.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(other):
+            h_out.copy_(dbuf, non_blocking=True)
+    stream.wait_stream(other)
+    b.record(stream)
+    b.synchronize()
+    rates["both"] = 2 * reps * nbytes / (a.elapsed_time(b) * 1e6)
+    del dbuf, dbuf2
     return rates
 
 
@@ -622,10 +637,20 @@ def run_ours(args, w, world, rank, local):
         barrier(world)
         per = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
         e2e_ms = max_over_ranks(marks[0].elapsed_time(marks[-1]), world) / args.steps
+        # what bounds a step: the device time of the same work, the copies at the measured link
+        # rates (both directions at once), and the pipeline's fill and drain (the first chunk's
+        # inputs and the last chunk's outputs, which nothing overlaps)
+        n_ch = len(ha.plan)
+        copies_ms = (h2d + d2h) / (link["both"] * 1e6)
+        fill_drain_ms = (h2d / n_ch) / (link["h2d"] * 1e6) + (d2h / n_ch) / (link["d2h"] * 1e6)
+        bound_ms = max(ms_step, copies_ms) + fill_drain_ms
         e2e = {"value": (f_fwd + f_bwd) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "replay_ms": {"median": statistics.median(per), "min": min(per), "max": max(per)},
-               "chunks": len(ha.plan), "host_link_gbs": link}
+               "chunks": n_ch, "host_link_gbs": link,
+               "bound_ms": {"device_step": ms_step, "copies_both_directions": copies_ms,
+                            "fill_and_drain": fill_drain_ms, "bound": bound_ms},
+               "median_over_device_step": statistics.median(per) / ms_step}
         assert fa.fa_get_error() == fa.FA_OK
 
     if rank != 0:
