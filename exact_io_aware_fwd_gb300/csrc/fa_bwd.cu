@@ -207,20 +207,30 @@ struct BwdLayout {
   static constexpr uint32_t kDS = kDO + 2 * kTile; // 128 keys x 128 queries bf16
   static constexpr uint32_t kLse = kDS + 32768;    // 2 stages x 128 floats
   static constexpr uint32_t kDelta = kLse + 1024;  // 2 stages x 128 floats
-  static constexpr uint32_t kBar = kDelta + 1024;
+  // d = 64: two slots of one dQ partial (128 rows x D fp32, the accumulator tile's layout) that
+  // the TMA unit adds into the accumulator (there is no room for them at d = 128)
+  static constexpr bool kBulkDQ = (D == 64);
+  static constexpr uint32_t kPart = 128u * D * 4u;
+  static constexpr uint32_t kStage = kDelta + 1024;
+  static constexpr uint32_t kBar = kStage + (kBulkDQ ? 2u * kPart : 0u);
   // kv_full, q_full[2], q_empty[2], do_full[2], do_empty[2], s_full, p_full, dp_full, ds_full,
   // dq_full, dq_empty, dkdv_full, mma_done, then the dQ claims' mode_full[2], mode_empty[2],
-  // first_stored[2]
-  static constexpr int kNumBars = 23;
+  // first_stored[2], then (d = 64) staged[2], stage_empty[2], the second dq_empty
+  static constexpr int kNumBars = 28;
   static constexpr uint32_t kMode = kBar + kNumBars * 8;  // 2 slots: how a drain writes
-  static constexpr uint32_t kTmemSlot = kMode + 8;
+  static constexpr uint32_t kKind = kMode + 8;            // 2 slots: the mode of a staged partial
+  static constexpr uint32_t kTmemSlot = kKind + 8;
   static constexpr uint32_t kAbort = kTmemSlot + 4;
   static constexpr uint32_t kBytes = kAbort + 4;
   // TMEM columns.  S^T (fp32) in [0, 128); P^T packed as bf16 pairs over the first half of each
   // 64-query half's own columns: queries 64h..64h+63 -> columns [64h, 64h + 32).  dP^T (fp32) in
   // [128, 256), dS^T packed the same way at 128 + [64h, 64h + 32); dQ_i (fp32, D columns) is
-  // accumulated over [128, 128 + D) once dK += dS^T Q has consumed dS^T.
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  // accumulated over [128, 128 + D) once dK += dS^T Q has consumed dS^T.  At d = 64 there are two
+  // such dP regions, [128, 256) for even and [256, 384) for odd query iterations, so that dP(i+1)
+  // need not wait for dQ(i) to be drained; dV and dK follow them.
+  static constexpr bool kDP2 = (D == 64);
+  static constexpr uint32_t kColS = 0, kColDP = 128;
+  static constexpr uint32_t kColDV = kDP2 ? 384 : 256, kColDK = kColDV + D;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -296,7 +306,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint64_t* mode_full = bars + 17;     // [2] the claim warp published how a drain writes
   uint64_t* mode_empty = bars + 19;    // [2] every drain warp took it (its drain has begun)
   uint64_t* first_stored = bars + 21;  // [2] every drain warp issued its stores of a first partial
+  uint64_t* staged = bars + 23;        // [2] (d = 64) every drain warp wrote its share of a slot
+  uint64_t* stage_empty = bars + 25;   // [2] (d = 64) the TMA unit has read the slot
+  // the drain of iteration it releases dq_empty_of(it): at d = 64 one barrier per dP region
+  auto dq_empty_of = [&](int it) { return (L::kDP2 && (it & 1)) ? bars + 27 : dq_empty; };
+  auto dp_col = [&](int it) { return L::kColDP + ((L::kDP2 && (it & 1)) ? 128u : 0u); };
   volatile int* mode_slot = reinterpret_cast<volatile int*>(sm + L::kMode);
+  volatile int* stage_kind = reinterpret_cast<volatile int*>(sm + L::kKind);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kTmemSlot);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kAbort);
   const Ctl ctl{abort_flag, a.status, a.timeout_ns};
@@ -361,9 +377,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P, dS, the release of dQ_i's tensor memory and the drain barriers are signalled by every
       // warp of the elementwise warpgroups
       uint32_t count = 1;
-      if (&bars[k] == p_full || &bars[k] == ds_full || &bars[k] == dq_empty ||
+      if (&bars[k] == p_full || &bars[k] == ds_full || &bars[k] == dq_empty || k == 27 ||
           &bars[k] == &mode_empty[0] || &bars[k] == &mode_empty[1] ||
-          &bars[k] == &first_stored[0] || &bars[k] == &first_stored[1])
+          &bars[k] == &first_stored[0] || &bars[k] == &first_stored[1] ||
+          &bars[k] == &staged[0] || &bars[k] == &staged[1])
         count = 4 * kGroups;
       mbar_init(&bars[k], count);
     }
@@ -458,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(s_full);
       };
       auto issue_dP = [&](int it) {  // dP^T = V_j dO_i^T
-        mma_ss_kmajor<D>(tmem + L::kColDP, desc_v, desc_do(it), idS, 0u);
+        mma_ss_kmajor<D>(tmem + dp_col(it), desc_v, desc_do(it), idS, 0u);
         mma_commit(dp_full);
       };
       auto issue_dV = [&](int it) {  // dV += P^T dO_i   (128 queries, 16 per MMA: +2 KB rows)
@@ -467,10 +484,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // dO_i is read by dP(i) and dV(i): its stage is released after whichever is issued last
       auto release_do = [&](int it) { mma_commit(&do_empty[it & 1]); };
       auto issue_dK_dQ = [&](int it) {
-        ts_chain(tmem + L::kColDK, tmem + L::kColDP, desc_q(it), it > 0 ? 1u : 0u);  // dK += dS^T Q_i
+        ts_chain(tmem + L::kColDK, tmem + dp_col(it), desc_q(it), it > 0 ? 1u : 0u);  // dK += dS^T Q_i
         mma_commit(&q_empty[it & 1]);
         if (kWithDQ) {  // dQ_i = dS K_j  (128 keys, 16 per MMA) over dP^T
-          mma_ss_mn_k128(tmem + L::kColDP, desc_ds, desc_k, idQ, 0u);
+          mma_ss_mn_k128(tmem + dp_col(it), desc_ds, desc_k, idQ, 0u);
           mma_commit(dq_full);
         }
       };
@@ -501,7 +518,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!(ok = mbar_wait(ds_full, it & 1, ctl))) break;
         tc_fence_after();
         issue_dK_dQ(it);
-        if (it + 1 < nIt) {
+        if (it + 1 < nIt && L::kDP2) {
+          // d = 64: dP(i+1) has a region of its own (dQ(i - 1)'s, drained before dS(i)), so it
+          // goes first, ahead of the P(i+1) that dV(i+1) waits for
+          if (!(ok = wait_do(it + 1))) break;
+          if (kWithDQ && it >= 1 && !(ok = mbar_wait(dq_empty_of(it - 1), ((it - 1) >> 1) & 1, ctl)))
+            break;
+          tc_fence_after();
+          issue_dP(it + 1);
+          if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl))) break;
+          tc_fence_after();
+          issue_dV(it + 1);
+          release_do(it + 1);
+          if (it + 2 < nIt) {
+            if (!(ok = wait_q(it + 2))) break;
+            tc_fence_after();
+            issue_S(it + 2);
+          }
+        } else if (it + 1 < nIt) {
           // dV(i+1) reads dO(i+1): its copy must have landed (P(i+1) does not depend on it)
           if (!(ok = mbar_wait(p_full, (it + 1) & 1, ctl) && wait_do(it + 1))) break;
           tc_fence_after();
@@ -522,34 +556,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       drain_wait(mma_done, 0, ctl);
     }
   } else if (warp == 2 || warp == 3) {
-    // ================= dQ claims (one thread of each warp; warp 2 the even iterations, warp 3
-    // the odd ones).  Claims each query tile and tells the drain warps whether to store its
-    // partial (the tile's first claimant) or add it (any later one, once the first one's stores
-    // are visible).  A claim is an acquiring atomic add on the tile's word, whose old value also
-    // says whether the first partial is stored yet.  An atomic from this SM waits behind the SM's
-    // own dQ additions in flight (thousands of cycles, about a tile period) and an acquiring one
-    // holds back its thread's later memory operations meanwhile, so each thread serves every
-    // other iteration and claims two drains ahead: iteration it at the start of the drain of it - 2
-    // (iteration 0 at the start, iteration 1 at the drain of 0).  Claims thus follow the order of
-    // the drains, and under the causal order (and the rotated non-causal one) the first claimant of
-    // a tile is the key tile that drains it first.  After the drain warps have issued a first
-    // partial's stores, a fence orders them before the record's bit 63.
-    if (kWithDQ && lane == 0 && nIt > warp - 2) {
-      const int par = static_cast<int>(warp) - 2;  // the iterations it with it % 2 == par
+    // ================= dQ claims (at d = 128 one thread of each warp, warp 2 the even iterations
+    // and warp 3 the odd ones; at d = 64 warp 2 alone).  Claims each query tile and tells the
+    // drain warps whether to store its partial (the tile's first claimant) or add it (any later
+    // one, once the first one's stores are visible).  A claim is an acquiring atomic add on the
+    // tile's word, whose old value also says whether the first partial is stored yet.  An atomic
+    // from this SM waits behind the SM's own dQ additions in flight (thousands of cycles, about a
+    // tile period) and an acquiring one holds back its thread's later memory operations meanwhile,
+    // so claims are made two drains ahead: iteration it at the start of the drain of it - 2
+    // (iteration 0 at the start, iteration 1 at the drain of 0), at d = 128 by two threads taking
+    // turns.  Claims thus follow the order of the drains, and under the causal order (and the
+    // rotated non-causal one) the first claimant of a tile is the key tile that drains it first.
+    // After the drain warps have issued a first partial's stores, a fence orders them before the
+    // record's bit 63.
+    constexpr int kClaimThreads = L::kBulkDQ ? 1 : 2;
+    const int par = static_cast<int>(warp) - 2;
+    if (kWithDQ && lane == 0 && par < kClaimThreads && nIt > par) {
       auto rec = [&](int it) { return &a.dq_cnt[ws_tile_of(head_of(it), tile_of(it))].word; };
-      int firsts = 0;  // first partials among this thread's iterations (phases of first_stored)
-      int prev_first = -1;  // the previous iteration of this thread, if it stored a first partial
+      int firsts0 = 0, firsts1 = 0;  // first partials of this thread per first_stored slot
+      int prev_first = -1;  // this thread's previous iteration, if it stored a first partial
+      auto first_done = [&](int it) -> bool {  // the drain of `it` stores a first partial
+        int& f = (it & 1) ? firsts1 : firsts0;
+        if (!mbar_wait(&first_stored[it & 1], f & 1, ctl)) return false;
+        ++f;
+        fence_acq_rel_gpu();  // the drain warps' stores (seen through first_stored) go first
+        red_add_relaxed_u64(rec(it), kDqStored);
+        return true;
+      };
       bool ok = true;
-      for (int it = par; ok && it < nIt; it += 2) {
+      for (int it = par; ok && it < nIt; it += kClaimThreads) {
         // claim time: the start of the drain of it - 2 (of 0 for iteration 1)
         if (it >= 1 && !(ok = mbar_wait(&mode_empty[it < 2 ? 0 : it & 1],
                                         it < 2 ? 0u : ((it - 2) >> 1) & 1, ctl)))
           break;
-        if (prev_first >= 0) {  // the drain of prev_first has begun: its stores are next
-          if (!(ok = mbar_wait(&first_stored[par], firsts & 1, ctl))) break;
-          ++firsts;
-          fence_acq_rel_gpu();  // the drain warps' stores (seen through first_stored) go first
-          red_add_relaxed_u64(rec(prev_first), kDqStored);
+        if (prev_first >= 0) {
+          if (!(ok = first_done(prev_first))) break;
           prev_first = -1;
         }
         const uint64_t old = atom_add_acquire_u64(rec(it), 1ull);
@@ -559,12 +600,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(&mode_full[it & 1]);
         if (first) prev_first = it;
       }
-      if (ok && prev_first >= 0) {  // the last iteration of this thread stored a first partial
-        if (mbar_wait(&first_stored[par], firsts & 1, ctl)) {
-          fence_acq_rel_gpu();
-          red_add_relaxed_u64(rec(prev_first), kDqStored);
+      if (ok && prev_first >= 0) first_done(prev_first);  // this thread's last iteration's
+    } else if (L::kBulkDQ && kWithDQ && lane == 0 && par == 1 && nIt > 0) {
+      // ================= dQ additions at d = 64 (warp 3): hands each staged partial to the TMA
+      // unit, which adds it into the accumulator (cp.reduce.async.bulk), so the drain warps never
+      // wait for the L2 to take their additions; a slot is released once the unit has read it
+      bool ok = true;
+      int prev_kind = -1;
+      for (int it = 0; it < nIt; ++it) {
+        const int s = it & 1;
+        if (!(ok = mbar_wait(&staged[s], (it >> 1) & 1, ctl))) break;
+        const int kind = stage_kind[s];
+        if (kind == kModeAdd) {
+          // the acquire of the first partial's bit (generic proxy) precedes these additions
+          fence_proxy_async_global();
+          bulk_reduce_add_f32(a.dq_acc + ws_tile_of(head_of(it), tile_of(it)) * 128 * D,
+                              sm + L::kStage + s * L::kPart, L::kPart);
+          bulk_commit();
         }
+        if (it >= 1) {  // the previous slot, once read
+          if (prev_kind == kModeAdd) {
+            if (kind == kModeAdd) bulk_wait_read1();
+            else bulk_wait_read0();
+          }
+          mbar_arrive(&stage_empty[(it - 1) & 1]);
+        }
+        prev_kind = kind;
       }
+      bulk_wait0();  // every addition performed before the CTA exits (aborted or not)
     }
   } else if (warp >= 4) {
     // ================= P, dS, the dQ drain and the epilogue: one thread per row of the tile,
@@ -577,9 +640,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool row_live = key < kv_len;
     const uint32_t lanes = (quad * 32u) << 16;
     const uint32_t tS = tmem + lanes + L::kColS + q0;
-    const uint32_t tDP = tmem + lanes + L::kColDP + q0;
     constexpr int kDC = D / kGroups;  // dQ columns drained by this group
-    const uint32_t tDQ = tmem + lanes + L::kColDP + kDC * grp;
+    // dP^T / dS^T and dQ columns of iteration it (two alternating regions at d = 64)
+    auto tDP_of = [&](int it) { return tmem + lanes + dp_col(it) + q0; };
+    auto tDQ_of = [&](int it) { return tmem + lanes + dp_col(it) + kDC * grp; };
     const float c2 = a.scale_log2;
 
     // dQ_i (query row r of the tile, this group's columns) into the fp32 accumulator: load,
@@ -611,6 +675,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_after();
       float* tile = a.dq_acc + ws_tile_of(qh, qt) * 128 * D;
       const int g0 = kGroups4 * grp;  // first 4-column group of this group's columns
+      const uint32_t tDQ = tDQ_of(it);
       uint32_t v[kDC];
       if constexpr (kDC == 64) {
         tmem_ld32(tDQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -624,7 +689,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       reg_fence(v);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
+      if (lane == 0) mbar_arrive(dq_empty_of(it));
+      if constexpr (L::kBulkDQ) {
+        // d = 64: a first partial is stored directly; any other goes to a shared-memory slot (the
+        // accumulator tile's layout) whose addition the TMA unit performs
+        const int ss = it & 1;
+        if (!mbar_wait_warp(&stage_empty[ss], ((it >> 1) & 1) ^ 1, ctl)) return false;
+        if (mode == kModeFirst) {
+#pragma unroll
+          for (int g = 0; g < kGroups4; ++g)
+            st_v4(tile + ((g0 + g) * 128 + r) * 4, __uint_as_float(v[4 * g]),
+                  __uint_as_float(v[4 * g + 1]), __uint_as_float(v[4 * g + 2]),
+                  __uint_as_float(v[4 * g + 3]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&first_stored[it & 1]);
+        } else {
+          const uint32_t slot = sbase + L::kStage + ss * L::kPart;
+#pragma unroll
+          for (int g = 0; g < kGroups4; ++g)
+            st_shared_v4(slot + (((g0 + g) * 128 + r) * 4) * 4, v[4 * g], v[4 * g + 1],
+                         v[4 * g + 2], v[4 * g + 3]);
+          fence_proxy_async_smem();  // the TMA unit reads the slot
+        }
+        __syncwarp();
+        if (lane == 0) {
+          stage_kind[ss] = mode;
+          mbar_arrive(&staged[ss]);
+        }
+        return true;
+      }
       if (mode == kModeFirst) {  // the tile's first partial: stored, whole lines per warp
 #pragma unroll
         for (int g = 0; g < kGroups4; ++g)
@@ -713,6 +806,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
       if (!(ok = mbar_wait_warp(dp_full, it & 1, ctl))) break;
       tc_fence_after();
+      const uint32_t tDP = tDP_of(it);
 #pragma unroll
       for (int c = 0; c < kQG / 32; ++c) {
         uint32_t dv[32];
