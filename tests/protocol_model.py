@@ -22,8 +22,9 @@ interleavings:
 A missing wait lets some interleaving read a stage before its copy lands; a release before the
 last reader lets the producer overwrite a stage that is still needed; both fail here.  The models
 follow the kernels' code (fa_fwd.cu: fwd_kernel's producer, MMA issuer and softmax warpgroups,
-dense and half-step; fa_bwd.cu: bwd_dkdv_kernel's producer, MMA issuer and elementwise
-warpgroups; fa_bwd_dq.cu: bwd_dq_kernel's) and must change with it.
+dense and half-step; fa_bwd.cu: bwd_dkdv_kernel's producer, MMA issuer, dQ claim threads, the
+d = 64 addition thread and elementwise warpgroups; fa_bwd_dq.cu: bwd_dq_kernel's) and must
+change with it.
 """
 
 from __future__ import annotations
@@ -391,41 +392,62 @@ def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, condition
 
 
 # ------------------------------------------------------------------------------------------
-# dK/dV kernel (bwd_dkdv_kernel with the dQ MMA and drain): one key tile, nit query iterations;
-# two Q (with its LSE, D rows) and two dO stages; `groups` elementwise warpgroups, each owning
-# its share of the query columns of S^T / dP^T and of the dQ columns, per 32-lane quadrant (the
-# d = 128 column layout: a group's dQ columns are its own dS columns).
+# dK/dV kernel (bwd_dkdv_kernel with the dQ MMA, the claims and the drain): one key tile, nit
+# query iterations; two Q (with its LSE, D rows) and two dO stages; `groups` elementwise
+# warpgroups, each owning its share of the query columns of S^T / dP^T and of the dQ columns,
+# per 32-lane quadrant.  Two layouts: d = 128 (one dP region that dQ_i reuses, dV(i+1) issued
+# before dP(i+1), two claim threads taking turns, dQ added by the drain warps) and d = 64 (two
+# dP regions for even and odd iterations, dP(i+1) issued before dV(i+1), one claim thread, the
+# added dQ partials staged in two shared-memory slots for the TMA unit's additions).
 
-def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional_drain=False):
+def dkdv(nit, seed, d64=False, groups=2, with_dq=True, bug=None, abort_at=None,
+         conditional_drain=False):
     """`bug` plants a protocol error (for the tests that show the checker catches it):
     "dv_before_do": dV(i+1) issued before waiting for dO(i+1)'s copy (a race once present in the
-    kernel); "early_q_release": Q_i's stage released before dK(i), its last reader.
-    ("early_do_release", dO(i+1)'s stage released right after dV(i+1) and before dP(i+1), is
-    harmless under this producer order: the producer refills that stage only after Q_(i+3)'s
-    stage, which dK(i+1) releases after dP(i+1) has run; the tests show that too.)
-    `abort_at`, `conditional_drain`: as for forward(); the roles then leave as the kernel's do.
-    Returns the Sim."""
+    kernel, d = 128 order); "early_q_release": Q_i's stage released before dK(i), its last
+    reader; "no_stage_wait" (d = 64): a drain writes a staging slot without waiting for the TMA
+    unit to have read it; "no_mode_wait": a drain takes the mode of its partial without waiting
+    for the claim.  ("early_do_release", dO(i+1)'s stage released right after dV(i+1) and before
+    dP(i+1) in the d = 128 order, is harmless under this producer order: the producer refills
+    that stage only after Q_(i+3)'s stage, which dK(i+1) releases after dP(i+1) has run; the
+    tests show that too.)  `abort_at`, `conditional_drain`: as for forward(); the roles then
+    leave as the kernel's do.  The claims' outcome (first claimant or not) is drawn at random:
+    the other key tiles are dq_claims' subject.  Returns the Sim."""
     sim = Sim(seed, abort_at)
     wait_ok = sim.wait_ok
     W = 4 * groups  # elementwise warps
+    dp2 = d64
+    bulk = d64 and with_dq
+    nclaim = 1 if d64 else 2
+    nreg = 2 if dp2 else 1
     kv_full = Bar(1, "kv_full")
     q_full = [Bar(1, f"q_full{s}") for s in range(2)]
     q_empty = [Bar(1, f"q_empty{s}") for s in range(2)]
     do_full = [Bar(1, f"do_full{s}") for s in range(2)]
     do_empty = [Bar(1, f"do_empty{s}") for s in range(2)]
     s_full, dp_full = Bar(1, "s_full"), Bar(1, "dp_full")
-    p_full, ds_full, dq_empty = Bar(W, "p_full"), Bar(W, "ds_full"), Bar(W, "dq_empty")
+    p_full, ds_full = Bar(W, "p_full"), Bar(W, "ds_full")
+    dq_empty = [Bar(W, f"dq_empty{x}") for x in range(nreg)]
     dq_full, dkdv_full = Bar(1, "dq_full"), Bar(1, "dkdv_full")
     mma_done = Bar(1, "mma_done")
+    mode_full = [Bar(1, f"mode_full{s}") for s in range(2)]
+    mode_empty = [Bar(W, f"mode_empty{s}") for s in range(2)]
+    first_stored = [Bar(W, f"first_stored{s}") for s in range(2)]
+    staged = [Bar(W, f"staged{s}") for s in range(2)]
+    stage_empty = [Bar(1, f"stage_empty{s}") for s in range(2)]
+    mode_slot = [None, None]
+    stage_kind = [None, None]
     KV = Buf("KV")
     Qst = [Buf(f"Q{s}") for s in range(2)]
     dOst = [Buf(f"dO{s}") for s in range(2)]
     cells = [(g, q) for g in range(groups) for q in range(4)]
-    Sreg = {c: Buf(f"S{c}") for c in cells}    # S^T, then P^T
-    DPreg = {c: Buf(f"DP{c}") for c in cells}  # dP^T, then dS^T, then dQ
+    Sreg = {c: Buf(f"S{c}") for c in cells}                                 # S^T, then P^T
+    DPreg = {(x, c): Buf(f"DP{x}{c}") for x in range(nreg) for c in cells}  # dP^T, dS^T, dQ
     DS = {c: Buf(f"dS{c}") for c in cells}     # dS in shared memory (A operand of dQ = dS K)
+    Stage = {(x, c): Buf(f"stage{x}{c}") for x in range(2) for c in cells}  # d = 64: staged dQ
     acc = {"dV": 0, "dK": 0}
-    drained = [[] for _ in cells]
+    drained = {c: [] for c in cells}
+    reg = (lambda it: it & 1) if dp2 else (lambda it: 0)
 
     def producer():
         if nit == 0:
@@ -481,7 +503,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
                 KV.read("KV")
                 dOst[it & 1].read(it, consume=True)
                 for c in cells:
-                    DPreg[c].write(("dP", it), readers=1)
+                    DPreg[(reg(it), c)].write(("dP", it), readers=1)
             sim.issue(fn)
             sim.issue(dp_full.arrive)
 
@@ -500,7 +522,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
         def issue_dK_dQ(it):
             def dk():
                 for c in cells:
-                    DPreg[c].read(("dS", it), consume=True)
+                    DPreg[(reg(it), c)].read(("dS", it), consume=True)
                 Qst[it & 1].read(it, consume=True)
                 assert acc["dK"] == it
                 acc["dK"] += 1
@@ -515,7 +537,7 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
                     for c in cells:
                         DS[c].read(("dS", it), consume=True)
                     for c in cells:
-                        DPreg[c].write(("dQ", it), readers=1)
+                        DPreg[(reg(it), c)].write(("dQ", it), readers=1)
                 sim.issue(dq)
                 sim.issue(dq_full.arrive)
 
@@ -541,11 +563,27 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
                     issue_S(1)
         it = 0
         while ok and it < nit:
-            ok = yield from wait_ok(ds_full, it & 1, it + 1)
-            if not ok:
+            if not (ok := (yield from wait_ok(ds_full, it & 1, it + 1))):
                 break
             issue_dK_dQ(it)
-            if it + 1 < nit:
+            if it + 1 < nit and dp2:
+                # d = 64: dP(i+1) goes into the region dQ(i-1) has left, ahead of dV(i+1)
+                ok = yield from wait_do(it + 1)
+                if ok and with_dq and it >= 1:
+                    p = it - 1
+                    ok = yield from wait_ok(dq_empty[reg(p)], (p >> 1) & 1, (p >> 1) + 1)
+                if not ok:
+                    break
+                issue_dP(it + 1)
+                if not (ok := (yield from wait_ok(p_full, (it + 1) & 1, it + 2))):
+                    break
+                issue_dV(it + 1)
+                release_do(it + 1)
+                if it + 2 < nit:
+                    if not (ok := (yield from wait_q(it + 2))):
+                        break
+                    issue_S(it + 2)
+            elif it + 1 < nit:
                 ok = yield from wait_ok(p_full, (it + 1) & 1, it + 2)
                 if ok and bug != "dv_before_do":
                     ok = yield from wait_do(it + 1)
@@ -553,21 +591,18 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
                     break
                 issue_dV(it + 1)
                 if bug == "dv_before_do":
-                    ok = yield from wait_do(it + 1)
-                    if not ok:
+                    if not (ok := (yield from wait_do(it + 1))):
                         break
                 if bug == "early_do_release":
                     release_do(it + 1)
                 if with_dq:
-                    ok = yield from wait_ok(dq_empty, it & 1, it + 1)
-                    if not ok:
+                    if not (ok := (yield from wait_ok(dq_empty[0], it & 1, it + 1))):
                         break
                 issue_dP(it + 1)
                 if bug != "early_do_release":
                     release_do(it + 1)
                 if it + 2 < nit:
-                    ok = yield from wait_q(it + 2)
-                    if not ok:
+                    if not (ok := (yield from wait_q(it + 2))):
                         break
                     issue_S(it + 2)
             it += 1
@@ -576,38 +611,114 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
         sim.issue(mma_done.arrive)
         yield from sim.drain(mma_done, 0)
 
-    def elementwise(c, k):
+    def claimer(par):
+        firsts = [0, 0]  # first partials of this thread per first_stored slot
+        prev_first = None
+
+        def first_done(it):
+            x = it & 1
+            if not (yield from wait_ok(first_stored[x], firsts[x] & 1, firsts[x] + 1)):
+                return False
+            firsts[x] += 1
+            return True
+
+        ok = True
+        for it in range(par, nit, nclaim):
+            # claim time: the start of the drain of it - 2 (of 0 for iteration 1)
+            if it >= 1:
+                bar, ph, cmp = ((mode_empty[0], 0, 1) if it < 2 else
+                                (mode_empty[it & 1], ((it - 2) >> 1) & 1, ((it - 2) >> 1) + 1))
+                if not (ok := (yield from wait_ok(bar, ph, cmp))):
+                    break
+            if prev_first is not None:
+                if not (ok := (yield from first_done(prev_first))):
+                    break
+                prev_first = None
+            first = sim.rng.random() < 0.5  # the tile's word (the other key tiles: dq_claims)
+            yield
+            mode_slot[it & 1] = (it, "first" if first else "add")
+            mode_full[it & 1].arrive()
+            if first:
+                prev_first = it
+        if ok and prev_first is not None:
+            yield from first_done(prev_first)
+
+    def reducer():
+        reads = []  # per addition issued, whether the unit has read its slot (in issue order)
+        prev_kind = None
+        for it in range(nit):
+            x = it & 1
+            if not (yield from wait_ok(staged[x], (it >> 1) & 1, (it >> 1) + 1)):
+                break
+            gg, kind = stage_kind[x]
+            assert gg == it
+            if kind == "add":
+                done = [False]
+                reads.append(done)
+
+                def bulk_read(it=it, x=x, done=done):
+                    for c in cells:
+                        Stage[(x, c)].read(("dQ", it), consume=True)
+                    done[0] = True
+                sim.copy(bulk_read)
+            if it >= 1:  # the previous slot, once read (wait_group.read 1 or 0)
+                if prev_kind == "add":
+                    keep = 1 if kind == "add" else 0  # the most recent addition may be pending
+                    while not all(d[0] for d in reads[:len(reads) - keep]):
+                        yield
+                stage_empty[(it - 1) & 1].arrive()
+            prev_kind = kind
+        while not all(d[0] for d in reads):  # every addition done before the CTA exits
+            yield
+
+    def elementwise(c):
         def drain(it):
+            if bug != "no_mode_wait":
+                if not (yield from wait_ok(mode_full[it & 1], (it >> 1) & 1, (it >> 1) + 1)):
+                    return False
+            slot_val = mode_slot[it & 1]
+            assert slot_val is not None and slot_val[0] == it, f"drain {it} took mode {slot_val}"
+            mode = slot_val[1]
+            mode_empty[it & 1].arrive()
             if not (yield from wait_ok(dq_full, it & 1, it + 1)):
                 return False
-            DPreg[c].read(("dQ", it), consume=True)
-            drained[k].append(it)
-            dq_empty.arrive()
+            DPreg[(reg(it), c)].read(("dQ", it), consume=True)
+            drained[c].append(it)
+            dq_empty[reg(it)].arrive()
+            if bulk:
+                x = it & 1
+                if bug != "no_stage_wait":
+                    if not (yield from wait_ok(stage_empty[x], ((it >> 1) & 1) ^ 1, it >> 1)):
+                        return False
+                if mode == "first":
+                    first_stored[it & 1].arrive()
+                else:
+                    Stage[(x, c)].write(("dQ", it), readers=1)
+                stage_kind[x] = (it, mode)
+                staged[x].arrive()
+            elif mode == "first":
+                first_stored[it & 1].arrive()
             return True
 
         ok = True
         for it in range(nit):
             s, ph = it & 1, (it >> 1) & 1
-            ok = yield from wait_ok(q_full[s], ph, (it >> 1) + 1)
-            if not ok:
+            if not (ok := (yield from wait_ok(q_full[s], ph, (it >> 1) + 1))):
                 break
-            Qst[s].read(it, consume=True)  # the LSE and D rows of this query tile
-            ok = yield from wait_ok(s_full, it & 1, it + 1)
-            if not ok:
+            Qst[s].read(it, consume=True)  # the LSE rows of this query tile
+            if not (ok := (yield from wait_ok(s_full, it & 1, it + 1))):
                 break
             Sreg[c].read(("S", it), consume=True)
             Sreg[c].write(("P", it), readers=1)
             p_full.arrive()
             if with_dq and it > 0:
-                ok = yield from drain(it - 1)
-                if not ok:
+                if not (ok := (yield from drain(it - 1))):
                     break
-            ok = yield from wait_ok(dp_full, it & 1, it + 1)
-            if not ok:
+            if not (ok := (yield from wait_ok(dp_full, it & 1, it + 1))):
                 break
-            DPreg[c].read(("dP", it), consume=True)
-            Qst[s].read(it, consume=True)
-            DPreg[c].write(("dS", it), readers=1)
+            DPreg[(reg(it), c)].read(("dP", it), consume=True)
+            Qst[s].read(it, consume=True)  # the D rows
+            DPreg[(reg(it), c)].write(("dS", it), readers=1)
             if with_dq:
                 DS[c].write(("dS", it), readers=1)
             ds_full.arrive()
@@ -618,13 +729,18 @@ def dkdv(nit, seed, groups=2, with_dq=True, bug=None, abort_at=None, conditional
             if ok:
                 assert acc["dV"] == nit and acc["dK"] == nit
 
-    sim.run([producer()] + [elementwise(c, k) for k, c in enumerate(cells)], mma())
+    agents = [producer()] + [elementwise(c) for c in cells]
+    if with_dq:
+        agents += [claimer(p) for p in range(nclaim) if p < nit]
+        if bulk:
+            agents.append(reducer())
+    sim.run(agents, mma())
     assert sim.exit_ops == 0, f"CTA exits with {sim.exit_ops} MMA operations queued"
     if not sim.abort:
         assert sim.exit_copies == 0, f"CTA exits with {sim.exit_copies} copies in flight"
         assert acc == {"dV": nit, "dK": nit}
         if with_dq:
-            assert all(d == list(range(nit)) for d in drained)
+            assert all(d == list(range(nit)) for d in drained.values())
     return sim
 
 

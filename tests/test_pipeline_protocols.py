@@ -1,5 +1,7 @@
 """CPU model check of the kernels' mbarrier pipelines (tests/protocol_model.py): the forward
-(128-key steps, block-sparse streams with gaps, the d = 64 half steps), the dK/dV kernel and the deterministic dQ kernel run their roles' waits, arrivals
+(128-key steps, block-sparse streams with gaps, the d = 64 half steps), the dK/dV kernel (its
+d = 128 and d = 64 layouts, with the dQ claims and, at d = 64, the staged TMA additions) and the
+deterministic dQ kernel run their roles' waits, arrivals
 and buffer reads and writes under many random interleavings (and the dK/dV kernel's CTAs their
 claims on the shared dQ accumulator), for every per-tile step count up to
 a few stages past the ring's length; no deadlock, no wait on a wrong phase, no read of a stage
@@ -38,12 +40,13 @@ def test_block_sparse_forward_protocol(S):
                 forward(None, S, False, seed, uses=uses)
 
 
+@pytest.mark.parametrize("d64", [False, True], ids=["d128", "d64"])
 @pytest.mark.parametrize("groups", [2, 4])
 @pytest.mark.parametrize("with_dq", [True, False])
-def test_dkdv_protocol(groups, with_dq):
+def test_dkdv_protocol(d64, groups, with_dq):
     for nit in range(0, 9):
         for seed in range(12):
-            dkdv(nit, seed, groups=groups, with_dq=with_dq)
+            dkdv(nit, seed, d64=d64, groups=groups, with_dq=with_dq)
 
 
 def test_deterministic_dq_protocol():
@@ -61,9 +64,11 @@ def _fails(fn):
     return False
 
 
-@pytest.mark.parametrize("bug", ["dv_before_do", "early_q_release"])
-def test_checker_catches_dkdv_protocol_errors(bug):
-    assert _fails(lambda seed: dkdv(6, seed, bug=bug))
+@pytest.mark.parametrize("d64,bug", [(False, "dv_before_do"), (False, "early_q_release"),
+                                     (True, "early_q_release"), (True, "no_stage_wait"),
+                                     (True, "no_mode_wait")])
+def test_checker_catches_dkdv_protocol_errors(d64, bug):
+    assert _fails(lambda seed: dkdv(6, seed, d64=d64, bug=bug))
 
 
 def test_early_do_release_is_harmless_under_this_producer_order():
@@ -113,15 +118,15 @@ def test_checker_catches_a_drain_only_when_already_aborted():
     assert any(sim.exit_copies > 0 for sim in _dq_abort_runs(conditional_drain=True))
 
 
-def _dkdv_abort_runs(with_dq, conditional_drain=False):
+def _dkdv_abort_runs(with_dq, conditional_drain=False, d64=False):
     import random
 
     rng = random.Random(13)
     for nit in (1, 2, 5, 8):
         for seed in range(5):
-            spins = dkdv(nit, seed, with_dq=with_dq).spins
+            spins = dkdv(nit, seed, d64=d64, with_dq=with_dq).spins
             for abort_at in sorted(rng.sample(range(1, max(2, spins + 1)), min(8, spins))):
-                yield dkdv(nit, seed, with_dq=with_dq, abort_at=abort_at,
+                yield dkdv(nit, seed, d64=d64, with_dq=with_dq, abort_at=abort_at,
                            conditional_drain=conditional_drain)
 
 
@@ -136,11 +141,12 @@ def _dq_abort_runs(conditional_drain=False):
                 yield dq_kernel(nb, seed, abort_at=abort_at, conditional_drain=conditional_drain)
 
 
+@pytest.mark.parametrize("d64", [False, True], ids=["d128", "d64"])
 @pytest.mark.parametrize("with_dq", [True, False])
-def test_dkdv_timeout_every_role_leaves(with_dq):
+def test_dkdv_timeout_every_role_leaves(with_dq, d64):
     """The dK/dV kernel's timeout path: a wait runs out at any point of any role; every role
-    leaves, and the CTA exits with no MMA queued and no copy in flight."""
-    for sim in _dkdv_abort_runs(with_dq):
+    leaves, and the CTA exits with no MMA queued and no copy (or TMA addition) in flight."""
+    for sim in _dkdv_abort_runs(with_dq, d64=d64):
         assert sim.abort and sim.exit_ops == 0 and sim.exit_copies == 0
 
 
