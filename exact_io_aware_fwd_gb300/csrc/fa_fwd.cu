@@ -232,7 +232,33 @@ __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
     }
   }
 
-  // ---- setup
+  // ---- setup.  Without a block mask the K/V stream's length is known here, and the thread that
+  // initialises the barriers also issues the copies that need no wait (the Q tiles and the first
+  // S K/V stages, all fresh) before the CTA-wide barrier that the tensor-memory allocation also
+  // waits for; the producer loop then starts at the first stage it has to wait for.
+  const int ntiles_q = (nb[1] > 0) ? 2 : 1;
+  auto issue_k = [&](int j, int kt) {
+    const int s = j % S;
+    mbar_arrive_expect_tx(&k_full[s], L::kTile);
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64,
+                  row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
+  };
+  auto issue_v = [&](int j, int kt) {
+    const int s = j % S;
+    mbar_arrive_expect_tx(&v_full[s], L::kTile);
+    for (int c = 0; c < D / 64; ++c)
+      tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64,
+                  row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
+  };
+  auto issue_q = [&]() {
+    mbar_arrive_expect_tx(q_full, ntiles_q * L::kTile);
+    for (int t = 0; t < ntiles_q; ++t)
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64,
+                    row_y(q_y0, q0 + 128 * t), row_z(q_z0, q0 + 128 * t));
+  };
+  const int n_pre = kSparse ? 0 : min(nb_max, S);  // K/V stages issued during the setup
   if (warp == 0 && lane == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
@@ -253,6 +279,13 @@ __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
+    if (n_pre > 0) {
+      issue_q();
+      for (int j = 0; j < n_pre; ++j) {
+        issue_k(j, j);
+        issue_v(j, j);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, L::kTmemCols);
@@ -270,28 +303,17 @@ __global__ void __launch_bounds__((kFwdThreads<D, kSparse, kVarlen>),
   if (warp == 0) {
     // ================= TMA producer
     if (lane == 0 && npos > 0) {
-      const int ntiles = (nb[1] > 0) ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, ntiles * L::kTile);
-      for (int t = 0; t < ntiles; ++t)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kQ + t * L::kTile + c * 16384, &tmQ, q_full, c * 64,
-                      row_y(q_y0, q0 + 128 * t), row_z(q_z0, q0 + 128 * t));
-      int jk = 0, jv = 0;  // K and V tiles whose copies have been issued
-      for (int j = 0; j < npos; ++j) {
+      if (n_pre == 0) issue_q();
+      int jk = n_pre, jv = n_pre;  // K and V tiles whose copies have been issued
+      for (int j = n_pre; j < npos; ++j) {
         const int s = j % S;
         const uint32_t ph = (j / S) & 1;
         const int kt = kSparse ? (__ldg(f_list + j) >> 2) : j;  // key tile at position j
         if (!mbar_wait(&k_empty[s], ph ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(&k_full[s], L::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kK + s * L::kTile + c * 16384, &tmK, &k_full[s], c * 64,
-                      row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
+        issue_k(j, kt);
         jk = j + 1;
         if (!mbar_wait(&v_empty[s], ph ^ 1, ctl)) break;
-        mbar_arrive_expect_tx(&v_full[s], L::kTile);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(sm + L::kV + s * L::kTile + c * 16384, &tmV, &v_full[s], c * 64,
-                      row_y(kv_y0, kt * 128), row_z(kv_z0, kt * 128));
+        issue_v(j, kt);
         jv = j + 1;
       }
       // No copy into this CTA's shared memory may still be in flight when the CTA exits, whether
