@@ -398,7 +398,7 @@ def forward(nsteps, S, half, seed, bug=None, uses=None, abort_at=None, condition
 # per 32-lane quadrant.  Two layouts: d = 128 (one dP region that dQ_i reuses, dV(i+1) issued
 # before dP(i+1), two claim threads taking turns, dQ added by the drain warps) and d = 64 (two
 # dP regions for even and odd iterations, dP(i+1) issued before dV(i+1), one claim thread, the
-# added dQ partials staged in two shared-memory slots for the TMA unit's additions).
+# added dQ partials but the last staged in two shared-memory slots for the TMA unit's additions).
 
 def dkdv(nit, seed, d64=False, groups=2, with_dq=True, bug=None, abort_at=None,
          conditional_drain=False):
@@ -646,7 +646,7 @@ def dkdv(nit, seed, d64=False, groups=2, with_dq=True, bug=None, abort_at=None,
     def reducer():
         reads = []  # per addition issued, whether the unit has read its slot (in issue order)
         prev_kind = None
-        for it in range(nit):
+        for it in range(nit - 1):  # (the last drain adds its partial itself)
             x = it & 1
             if not (yield from wait_ok(staged[x], (it >> 1) & 1, (it >> 1) + 1)):
                 break
@@ -685,7 +685,7 @@ def dkdv(nit, seed, d64=False, groups=2, with_dq=True, bug=None, abort_at=None,
             DPreg[(reg(it), c)].read(("dQ", it), consume=True)
             drained[c].append(it)
             dq_empty[reg(it)].arrive()
-            if bulk:
+            if bulk and it + 1 < nit:
                 x = it & 1
                 if bug != "no_stage_wait":
                     if not (yield from wait_ok(stage_empty[x], ((it >> 1) & 1) ^ 1, it >> 1)):
