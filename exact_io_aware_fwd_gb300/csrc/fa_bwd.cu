@@ -768,6 +768,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // masks; every other tile (the test is uniform over the CTA) skips them
       const bool masked = diag || (j * 128 + 128 > kv_len);
       uint32_t p[kQG / 2];
+      // d = 64 has the registers to keep P in fp32 for dS (no unpacking of the bf16 pairs; dS
+      // then uses the unrounded P): measured on GB300, dK/dV 0.915 -> 0.892 ms at 64x16x1024x64
+      constexpr bool kPf = (D == 64);
+      float pf[kPf ? kQG : 1];
       auto p_from_s = [&](auto kMask) {
 #pragma unroll
         for (int c = 0; c < kQG / 32; ++c) {
@@ -793,6 +797,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             p[16 * c + 2 * e] = pack_bf16(x[0], x[1]);
             p[16 * c + 2 * e + 1] = pack_bf16(x[2], x[3]);
+            if constexpr (kPf) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) pf[ql + u] = x[u];
+            }
           }
         }
       };
@@ -827,8 +835,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                  make_float2(d4.x, d4.y));
           const float2 t1 = add2(make_float2(__uint_as_float(dv[4 * e + 2]), __uint_as_float(dv[4 * e + 3])),
                                  make_float2(d4.z, d4.w));
-          const float2 u0 = mul2(make_float2(bf16_lo(pa), bf16_hi(pa)), t0);
-          const float2 u1 = mul2(make_float2(bf16_lo(pb), bf16_hi(pb)), t1);
+          const float2 p0 = kPf ? make_float2(pf[ql], pf[ql + 1]) : make_float2(bf16_lo(pa), bf16_hi(pa));
+          const float2 p1 = kPf ? make_float2(pf[ql + 2], pf[ql + 3]) : make_float2(bf16_lo(pb), bf16_hi(pb));
+          const float2 u0 = mul2(p0, t0);
+          const float2 u1 = mul2(p1, t1);
           ds[2 * e] = pack_bf16(u0.x, u0.y);
           ds[2 * e + 1] = pack_bf16(u1.x, u1.y);
         }
