@@ -1,5 +1,5 @@
 """Shared helpers of the GPU parity tests: run the CUDA path through the C ABI, run the fp64
-oracle on the same (bf16-rounded) inputs, and compare with the tolerances of the benchmark spec:
+oracle on the same (bf16-rounded) inputs, and compare with the stated tolerances:
 
   O    max-abs error <= 1e-2 (before the output's bf16 rounding, see compare_slice) and
        relative Frobenius error <= 5e-3
