@@ -34,6 +34,10 @@ SMALL = [
     (2, 1, 517, 128, False, (300, 517), 3.0, None),
     (2, 2, 389, 64, True, (1, 389), 2.0, None),
     (1, 2, 640, 128, False, None, 3.0, 0.05),
+    # d = 64 with large logits: the half-step forward's running max moves by large amounts, and
+    # the dK/dV kernel's dS uses the unrounded P
+    (2, 1, 517, 64, False, (300, 517), 3.0, None),
+    (1, 2, 1024, 64, True, None, 4.0, None),
 ]
 
 
